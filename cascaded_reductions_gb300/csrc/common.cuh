@@ -1,0 +1,75 @@
+// Shared device helpers and internal launcher declarations for librf.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rf.h"
+
+namespace rf {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- loads ----
+// 16-byte streaming load through the non-coherent path; not kept in L1 (every
+// byte is read once), with a 256-byte L2 prefetch hint for the sequential
+// stream that follows.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// bf16 pair packed in a 32-bit word -> two floats (exact widening).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> bf16 pair, round to nearest even (hardware cvt).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int WIDTH>
+__device__ __forceinline__ float group_max(float x) {
+#pragma unroll
+  for (int o = WIDTH / 2; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+  for (int o = WIDTH / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline rf_status launch_status() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? RF_OK : RF_ERR_CUDA;
+}
+
+// ------------------------------------------------------------ launchers ----
+// Each returns RF_OK or RF_ERR_CUDA; arguments were validated by the C ABI.
+rf_status launch_decode_split(const void* q, const void* k, const void* v, int R, int L, int D,
+                              int S, float scale, int dtype, float* seg_m, float* seg_l,
+                              float* seg_acc, cudaStream_t st);
+rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc, int R,
+                             int S, int D, void* out, int out_dtype, float* lse, cudaStream_t st);
+rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int renormalize,
+                              int32_t* idx, float* w, cudaStream_t st);
+rf_status launch_absmax_quant(const void* x, int M, int K, uint8_t* xq, float* sx,
+                              cudaStream_t st);
+rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                          int M, int N, int K, void* y, cudaStream_t st);
+rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
+                         int causal, float scale, void* out, float* lse, cudaStream_t st);
+rf_status read_device_error(int* status, cudaStream_t st);
+
+}  // namespace rf

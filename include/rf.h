@@ -1,0 +1,190 @@
+/*
+ * rf.h -- C ABI of librf.so: single-pass fused cascaded reductions on GB300.
+ *
+ * A cascaded reduction is a chain of reductions in which each stage needs
+ * the finished result of the one before (RedFuser episode transcript, cue 9:
+ * safe softmax's row max, then the exp-sum denominator, then the divide;
+ * cue 11: softmax then top-k for MoE routing, abs-max then FP8 quantisation
+ * then GEMM).  Every call below computes such a chain in one pass over its
+ * input by carrying a running state and rescaling stale partials when an
+ * earlier stage's result changes (transcript cues 15-21 and 31; the episode
+ * viz page's widgets "Online softmax, step by step" and "Merging partial
+ * states across blocks (FlashDecoding-style)").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named as tensors are DEVICE pointers (CUDA global memory) unless
+ *   stated otherwise.  The caller owns every buffer; the library allocates
+ *   nothing and frees nothing.
+ * - All tensors are dense, row-major and contiguous in the shapes given.
+ * - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ *   default stream).  Calls only enqueue work: they are asynchronous and
+ *   stream-ordered, and never synchronise.
+ * - Arguments are checked on the host before anything is launched.  A bad
+ *   argument returns its status code with nothing enqueued and no output
+ *   touched.  A failed launch returns RF_ERR_CUDA.  Nothing aborts, prints or
+ *   throws across this boundary.
+ * - Device pointers must be 16-byte aligned (RF_ERR_MISALIGNED otherwise).
+ * - Calls are thread-safe; the library keeps no per-call global state.
+ */
+#ifndef RF_H
+#define RF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RF_OK = 0,
+  RF_ERR_INVALID_ARG = 1,   /* null pointer, size <= 0, k > E, S < 1, ...     */
+  RF_ERR_UNSUPPORTED = 2,   /* a valid request outside the supported set      */
+  RF_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned               */
+  RF_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed    */
+  RF_ERR_TIMEOUT = 5        /* a bounded on-device wait gave up (see below)   */
+} rf_status;
+
+typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* rf_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int rf_version(void);
+
+/*
+ * rf_attn_decode_split -- split-KV decode attention, producer of segment
+ * states (the Multi-Segment strategy: transcript cue 39; viz page widget
+ * "Single-Segment vs Multi-Segment").
+ *
+ * For each row r (r = b*H + h) and each segment s of its L keys, the kernel
+ * streams the segment's K and V rows once and keeps the running state of
+ * transcript cues 15-19 and 31:
+ *   m' = max(m, max_j s_j),   c = exp(m - m'),
+ *   l' = c*l + sum_j exp(s_j - m'),   acc' = c*acc + sum_j exp(s_j - m') v_j,
+ * with scores s_j = scale * <q_r, k_j>.  It writes the unnormalised state.
+ *
+ *   q        [R, D]      dtype          query rows
+ *   k, v     [R, L, D]   dtype          keys / values of each row
+ *   R, L, D  rows, keys per row, head dim
+ *   S        number of segments, >= 1.  Segment s holds the keys
+ *            [s*c, min(L, (s+1)*c)), c = ceil(L/S).  S > L is allowed: a
+ *            segment with no keys gets the identity state (-inf, 0, 0)
+ *            (transcript cues 27 and 29: the monoid's identity element).
+ *   scale    score scale (1/sqrt(D) for attention)
+ *   dtype    RF_F32 with D = 64, or RF_BF16 with D = 128
+ *   seg_m    [R, S]      fp32 out       segment max of the scores, natural-log units
+ *   seg_l    [R, S]      fp32 out       sum_j exp(s_j - seg_m)
+ *   seg_acc  [R, S, D]   fp32 out       sum_j exp(s_j - seg_m) * v_j
+ * Errors: RF_ERR_INVALID_ARG for null pointers, R, L, D <= 0, S < 1 or a
+ * non-finite scale; RF_ERR_UNSUPPORTED for any other (dtype, D) pair.
+ */
+rf_status rf_attn_decode_split(const void* q, const void* k, const void* v,
+                               int R, int L, int D, int S, float scale, int dtype,
+                               float* seg_m, float* seg_l, float* seg_acc,
+                               void* stream);
+
+/*
+ * rf_state_merge -- combine the S segment states of each row and normalise
+ * (transcript cue 21: two partial states, each with its own max, combine with
+ * the same rescaling; viz page widget "Merging partial states across blocks").
+ *   M = max_s m_s;  w_s = exp(m_s - M) (0 for an identity state);
+ *   l = sum_s w_s l_s;  acc = sum_s w_s acc_s;  out = acc / l;  lse = M + ln l.
+ *
+ *   seg_m, seg_l, seg_acc   as written by rf_attn_decode_split
+ *   R, S, D                 rows, segments, head dim (D = 64 or 128)
+ *   out        [R, D]       out_dtype out (RF_F32 or RF_BF16, round to nearest even)
+ *   lse        [R]          fp32 out, may be NULL
+ * Errors: RF_ERR_INVALID_ARG for null inputs/out, R, S, D <= 0;
+ * RF_ERR_UNSUPPORTED for D not in {64, 128} or S > 1024.
+ * A row whose S states are all identity states gives NaN (it had no keys).
+ */
+rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc,
+                         int R, int S, int D, void* out, int out_dtype, float* lse,
+                         void* stream);
+
+/*
+ * rf_attn_prefill -- causal prefill attention, GEMM -> online softmax -> GEMM
+ * (transcript cue 9: attention stacks a GEMM, then softmax, then another GEMM;
+ * cue 31: the incremental form sits at the block level of the reduction tree).
+ * Each 128-row query tile streams its K/V tiles once: S = Q K^T * scale on
+ * the tensor cores, running (m, l) per row, O = c*O + P V, out = O / l.
+ *
+ *   q, k, v   [B, H, N, D]  bf16        D = 128
+ *   causal    1: query i sees keys 0..i (top-left aligned); 0: all keys
+ *   scale     score scale (1/sqrt(D))
+ *   out       [B, H, N, D]  bf16 out
+ *   lse       [B, H, N]     fp32 out (m + ln l, natural log), may be NULL
+ * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
+ * RF_ERR_UNSUPPORTED unless D = 128 and N % 128 == 0.
+ */
+rf_status rf_attn_prefill(const void* q, const void* k, const void* v,
+                          int B, int H, int N, int D, int causal, float scale,
+                          void* out, float* lse, void* stream);
+
+/*
+ * rf_softmax_topk -- MoE routing: softmax over experts, then top-k, from one
+ * read of each token's logits (transcript cue 11; "Online normalizer
+ * calculation for softmax", abstract: softmax and top-k fused).
+ *
+ *   logits  [T, E]  fp32
+ *   k       experts per token, 1 <= k <= min(E, 32)
+ *   renormalize  1: w_i = p_i / sum_{j in top-k} p_j;  0: w_i = p_i
+ *   idx     [T, k]  int32 out  expert indices, ordered by logit descending,
+ *                              equal logits by lower index first
+ *   w       [T, k]  fp32 out   routing weights in the same order
+ * Errors: RF_ERR_INVALID_ARG for null pointers, T, E <= 0, k < 1 or k > E;
+ * RF_ERR_UNSUPPORTED for E > 1024 or k > 32.
+ */
+rf_status rf_softmax_topk(const float* logits, int T, int E, int k, int renormalize,
+                          int32_t* idx, float* w, void* stream);
+
+/*
+ * rf_absmax_quant_fp8_gemm -- FP8 per-token quantisation then GEMM
+ * (transcript cue 33: the token's abs-max, then the GEMM over values scaled
+ * by FP8max / absmax).  Two kernels, enqueued back to back:
+ *   1. one pass over each row of X: amax = max |x|, sx = fp32(amax / 448),
+ *      xq = e4m3(fp32(x / sx)) rounded to nearest even, saturating at +-448;
+ *      a row with amax = 0 gets sx = 0 and zero codes;
+ *   2. Y = (Xq . Wq^T) * sx[m] * sw[n], fp32 accumulation on the FP8 tensor
+ *      cores, rounded to bf16.
+ *
+ *   x    [M, K]  bf16           activations
+ *   wq   [N, K]  e4m3 codes     weights (K-contiguous storage of W [K, N])
+ *   sw   [N]     fp32           per-output-column weight scales
+ *   xq   [M, K]  e4m3 codes out
+ *   sx   [M]     fp32 out       per-token scales
+ *   y    [M, N]  bf16 out
+ * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
+ * RF_ERR_UNSUPPORTED unless K % 128 == 0, M % 128 == 0, N % 256 == 0 and
+ * K <= 65536.
+ */
+rf_status rf_absmax_quant_fp8_gemm(const void* x, int M, int K,
+                                   const uint8_t* wq, const float* sw, int N,
+                                   uint8_t* xq, float* sx, void* y, void* stream);
+
+/* Phase 1 of rf_absmax_quant_fp8_gemm alone (same arguments and rules;
+ * any K % 8 == 0 is supported). */
+rf_status rf_absmax_quant_e4m3(const void* x, int M, int K, uint8_t* xq, float* sx,
+                               void* stream);
+
+/* Phase 2 of rf_absmax_quant_fp8_gemm alone (same arguments and rules). */
+rf_status rf_fp8_gemm_scaled(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                             const float* sw, int M, int N, int K, void* y, void* stream);
+
+/*
+ * rf_device_error -- status of the bounded on-device waits.  The
+ * tensor-core kernels wait on shared-memory barriers with an iteration
+ * limit; a wait that runs out records RF_ERR_TIMEOUT in a device word and
+ * the kernel returns early instead of hanging.  This call synchronises
+ * `stream`, reads that word into *status (RF_OK if no wait ran out), clears
+ * it, and returns RF_OK, or RF_ERR_CUDA if the read failed.
+ */
+rf_status rf_device_error(int* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RF_H */

@@ -1,0 +1,140 @@
+"""The C ABI library builds, loads and exports every symbol include/rf.h
+declares; host-side argument checks return their codes without a GPU.
+
+These run on a CPU-only machine: every call below is rejected by the host
+validation before any CUDA call is made.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from cascaded_reductions_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(rf_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("rf_attn_decode_split", "rf_state_merge", "rf_attn_prefill", "rf_softmax_topk",
+              "rf_absmax_quant_fp8_gemm", "rf_status_string", "rf_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    lib.rf_status_string.restype = ctypes.c_char_p
+    assert lib.rf_status_string(0) == b"RF_OK"
+    assert lib.rf_status_string(2) == b"RF_ERR_UNSUPPORTED"
+    assert lib.rf_status_string(99) == b"RF_ERR_UNKNOWN"
+    assert lib.rf_version() >= 10000
+
+
+P = ctypes.c_void_p
+FAKE = P(0x10000)          # aligned, never dereferenced: calls are rejected first
+ODD = P(0x10004)           # 4-byte aligned only
+NULL = P(0)
+F = ctypes.c_float
+
+
+def test_decode_split_validation(lib):
+    f = lib.rf_attn_decode_split
+    args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, o.get("R", 4), o.get("L", 100), o.get("D", 128),
+                        o.get("S", 4), F(o.get("scale", 0.1)), o.get("dtype", 1),
+                        FAKE, FAKE, o.get("acc", FAKE), NULL]
+    assert f(*args(q=NULL)) == 1
+    assert f(*args(R=0)) == 1
+    assert f(*args(L=-1)) == 1
+    assert f(*args(S=0)) == 1
+    assert f(*args(scale=float("inf"))) == 1
+    assert f(*args(dtype=7)) == 1
+    assert f(*args(D=64)) == 2            # bf16 with D=64 unsupported
+    assert f(*args(dtype=0)) == 2         # fp32 with D=128 unsupported
+    assert f(*args(q=ODD)) == 3
+    assert f(*args(acc=ODD)) == 3
+
+
+def test_merge_validation(lib):
+    f = lib.rf_state_merge
+    base = dict(m=FAKE, R=4, S=8, D=128, out=FAKE, od=1)
+    args = lambda **o: [o.get("m", FAKE), FAKE, o.get("acc", FAKE), o.get("R", 4), o.get("S", 8),
+                        o.get("D", 128), o.get("out", FAKE), o.get("od", 1), NULL, NULL]
+    assert f(*args(m=NULL)) == 1
+    assert f(*args(out=NULL)) == 1
+    assert f(*args(S=0)) == 1
+    assert f(*args(od=5)) == 1
+    assert f(*args(D=96)) == 2
+    assert f(*args(S=2000)) == 2
+    assert f(*args(out=ODD)) == 3
+    assert base
+
+
+def test_topk_validation(lib):
+    f = lib.rf_softmax_topk
+    args = lambda **o: [o.get("x", FAKE), o.get("T", 10), o.get("E", 64), o.get("k", 2), 1,
+                        FAKE, FAKE, NULL]
+    assert f(*args(x=NULL)) == 1
+    assert f(*args(T=0)) == 1
+    assert f(*args(k=0)) == 1
+    assert f(*args(k=65)) == 1            # k > E
+    assert f(*args(E=2048, k=4)) == 2
+    assert f(*args(E=100, k=40)) == 2     # k > 32
+    assert f(*args(x=ODD)) == 3
+
+
+def test_quant_gemm_validation(lib):
+    f = lib.rf_absmax_quant_fp8_gemm
+    args = lambda **o: [o.get("x", FAKE), o.get("M", 256), o.get("K", 512), FAKE, FAKE,
+                        o.get("N", 256), FAKE, FAKE, FAKE, NULL]
+    assert f(*args(x=NULL)) == 1
+    assert f(*args(M=0)) == 1
+    assert f(*args(K=100)) == 2
+    assert f(*args(N=100)) == 2
+    assert f(*args(M=100)) == 2
+    assert f(*args(x=ODD)) == 3
+    q = lib.rf_absmax_quant_e4m3
+    assert q(NULL, 4, 64, FAKE, FAKE, NULL) == 1
+    assert q(FAKE, 4, 60, FAKE, FAKE, NULL) == 2
+    assert q(ODD, 4, 64, FAKE, FAKE, NULL) == 3
+
+
+def test_prefill_validation(lib):
+    f = lib.rf_attn_prefill
+    args = lambda **o: [FAKE, FAKE, FAKE, o.get("B", 1), 2, o.get("N", 256), o.get("D", 128), 1,
+                        F(0.1), o.get("out", FAKE), NULL, NULL]
+    assert f(*args(out=NULL)) == 1
+    assert f(*args(B=0)) == 1
+    assert f(*args(D=64)) == 2
+    assert f(*args(N=200)) == 2
+    assert f(*args(out=ODD)) == 3
+
+
+def test_device_error_null(lib):
+    assert lib.rf_device_error(NULL, NULL) == 1
+
+
+def test_binding_declares_every_symbol():
+    """The Python binding wraps every entry point the header declares."""
+    import cascaded_reductions_gb300 as rf
+    assert set(rf._SIGNATURES) == set(declared_symbols())

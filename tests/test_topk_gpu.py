@@ -1,0 +1,65 @@
+"""Parity of rf_softmax_topk with the oracle through the C ABI.
+
+Indices bit-exact (ties by lower expert index), weights within the fp32
+tolerance.  Both routing workloads at full size ([16384 x 256] top-8 and
+[65536 x 64] top-2, element by element), plus edge cases: constructed ties,
+E = 2 with k = 1, E not a multiple of 4, k = E, k = 32, E = 1024, T = 1,
+and renormalize off.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close_f32
+from oracle import routing as Rt
+import synthetic_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rf():
+    import cascaded_reductions_gb300 as m
+    return m
+
+
+def check(rf, x, k, renorm, what):
+    idx, w = rf.softmax_topk(x.cuda(), k, renorm)
+    torch.cuda.synchronize()
+    ridx, rw = Rt.softmax_topk(x.numpy(), k, renorm)
+    gi = idx.cpu().numpy()
+    bad = np.argwhere(gi != ridx)
+    assert bad.size == 0, f"{what}: {len(bad)} index mismatches, first {bad[0]}: {gi[bad[0][0]]} vs {ridx[bad[0][0]]}"
+    assert_close_f32(w.cpu().numpy(), rw, what)
+
+
+@pytest.mark.parametrize("name", ["route_256", "route_64"])
+def test_full_size(rf, name):
+    cfg = si.FULL[name]
+    x = si.routing_logits(cfg["T"], cfg["E"], seed=si.SEEDS[name])
+    check(rf, x, cfg["k"], True, name)
+
+
+@pytest.mark.parametrize("E,k", [(2, 1), (2, 2), (3, 2), (33, 5), (64, 16), (64, 17), (100, 32),
+                                 (128, 8), (130, 3), (256, 32), (511, 9), (1024, 32), (1024, 1)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_shapes(rf, E, k, renorm):
+    x = si.routing_logits(37, E, seed=E * 7 + k)
+    check(rf, x, k, renorm, f"E={E} k={k}")
+
+
+def test_ties_lower_index_first(rf):
+    T, E = 64, 256
+    g = torch.Generator().manual_seed(9)
+    # few distinct values -> many exact ties, including at the k-th place
+    x = torch.randint(-3, 4, (T, E), generator=g).float()
+    x[5] = 0.0
+    check(rf, x, 8, True, "ties")
+    x2 = torch.randint(0, 2, (T, 64), generator=g).float()
+    check(rf, x2, 2, False, "ties E=64")
+
+
+def test_single_token(rf):
+    x = si.routing_logits(1, 256, seed=1)
+    check(rf, x, 8, True, "T=1")

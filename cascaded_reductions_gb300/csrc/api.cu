@@ -47,7 +47,6 @@ rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* se
   if (R <= 0 || S <= 0 || D <= 0) return RF_ERR_INVALID_ARG;
   if (out_dtype != RF_F32 && out_dtype != RF_BF16) return RF_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return RF_ERR_UNSUPPORTED;
-  if (S > 1024) return RF_ERR_UNSUPPORTED;
   if (!rf::aligned16(seg_acc) || !rf::aligned16(out)) return RF_ERR_MISALIGNED;
   return rf::launch_state_merge(seg_m, seg_l, seg_acc, R, S, D, out, out_dtype, lse,
                                 as_stream(stream));

@@ -71,5 +71,8 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
 rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
                          int causal, float scale, void* out, float* lse, cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);
+// read and clear the bounded-wait status word of each tensor-core kernel file
+rf_status gemm_take_status(int* status);
+rf_status prefill_take_status(int* status);
 
 }  // namespace rf

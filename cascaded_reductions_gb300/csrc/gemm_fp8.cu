@@ -1,12 +1,227 @@
-// FP8 GEMM with per-row x per-column scale epilogue (phase 2 of the abs-max ->
-// quantise -> GEMM cascade).  Placeholder until the tcgen05 kernel lands.
-#include "common.cuh"
+// FP8 GEMM with a per-row x per-column scale epilogue: phase 2 of the
+// abs-max -> quantise -> GEMM cascade (RedFuser episode transcript, cue 33;
+// cue 5: every GEMM output is a sum reduction along K).
+//
+//   Y[m, n] = bf16( (sum_k dec(Xq[m,k]) dec(Wq[n,k])) * sx[m] * sw[n] )
+//
+// Persistent, warp-specialised tcgen05 kernel, one CTA per SM:
+//   warp 0      TMA producer: 128x128-byte tiles of Xq and 256x128-byte tiles
+//               of Wq (128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and issues tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) from
+//               one thread, committing each stage back to the producer and
+//               each finished accumulator to the epilogue;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (each thread one
+//               row, 32 columns at a time), scale by sx[row] * sw[col],
+//               round to bf16, store; then hand the accumulator back, so the
+//               next tile's MMAs overlap this tile's epilogue.
+// Output tiles are 128 x 256; CTAs walk tiles t = blockIdx.x + i*gridDim.x.
+// Every barrier wait is bounded (see tc_common.cuh).
+
+#include <cuda_bf16.h>
+
+#include "tc_common.cuh"
 
 namespace rf {
+namespace {
 
-rf_status launch_fp8_gemm(const uint8_t*, const float*, const uint8_t*, const float*, int, int,
-                          int, void*, cudaStream_t) {
-  return RF_ERR_UNSUPPORTED;
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;                       // bytes = e4m3 elements per stage
+constexpr int UMMA_K = 32;                    // K of one kind::f8f6f4 MMA
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;              // 16 KiB
+constexpr int B_BYTES = BN * BK;              // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;             // two accumulators
+constexpr int THREADS = 192;
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(Shared) + 1024;
+
+__global__ void __launch_bounds__(THREADS, 1)
+fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const float* __restrict__ sx, const float* __restrict__ sw,
+                __nv_bfloat16* __restrict__ y, int M, int N, int K) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Shared* sh = reinterpret_cast<Shared*>(smem + (size_t)STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int tiles_n = N / BN;
+  const int num_tiles = (M / BM) * tiles_n;
+  const int num_k = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&sh->full[s], 1);
+      tc::mbar_init(&sh->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&sh->acc_full[b], 1);
+      tc::mbar_init(&sh->acc_empty[b], 4);
+    }
+    sh->abort = 0;
+    tc::fence_barrier_init();
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) tc::tmem_alloc(&sh->tmem_base, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = sh->tmem_base;
+  volatile int* abort = &sh->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer ----
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x) {
+        const int tm = tile / tiles_n, tn = tile - (tile / tiles_n) * tiles_n;
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort)) break;
+          uint8_t* a = smem + (size_t)s * STAGE_BYTES;
+          tc::mbar_arrive_expect_tx(&sh->full[s], STAGE_BYTES);
+          tc::tma_load_2d(a, &tmA, &sh->full[s], kb * BK, tm * BM);
+          tc::tma_load_2d(a + A_BYTES, &tmB, &sh->full[s], kb * BK, tn * BN);
+        }
+      }
+      // On an abort, let the copies already issued land before the CTA exits.
+      if (*abort) {
+        for (int s = 0; s < STAGES; ++s) {
+          const unsigned long long t0 = tc::globaltimer_ns();
+          while (!tc::mbar_try_wait(&sh->full[s], 0) && !tc::mbar_try_wait(&sh->full[s], 1) &&
+                 tc::globaltimer_ns() - t0 < tc::kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
+      uint32_t it = 0, t = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x, ++t) {
+        const int buf = t & 1;
+        const uint32_t bph = (t >> 1) & 1u;
+        if (!tc::mbar_wait(&sh->acc_empty[buf], bph ^ 1u, abort)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!tc::mbar_wait(&sh->full[s], ph, abort)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a = tc::smem_u32(smem + (size_t)s * STAGE_BYTES);
+          const uint64_t adesc = tc::sdesc_sw128(a, 16, 1024);
+          const uint64_t bdesc = tc::sdesc_sw128(a + A_BYTES, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            // advance the start address by k*32 bytes inside the swizzle atom
+            tc::mma_f8f6f4_ss(d, adesc + (uint64_t)(k * UMMA_K / 16), bdesc + (uint64_t)(k * UMMA_K / 16),
+                              idesc, (kb | k) != 0);
+          }
+          tc::mma_commit(&sh->empty[s]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&sh->acc_full[buf]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue ----
+    const int quarter = warp & 3;              // TMEM lanes this warp may access
+    const int r = quarter * 32 + lane;         // row within the tile
+    uint32_t t = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
+      const int buf = t & 1;
+      const uint32_t bph = (t >> 1) & 1u;
+      if (!tc::mbar_wait(&sh->acc_full[buf], bph, abort)) break;
+      tc::fence_after_sync();
+      const int tm = tile / tiles_n, tn = tile - (tile / tiles_n) * tiles_n;
+      const int row = tm * BM + r;
+      const float srow = sx[row];
+      __nv_bfloat16* yrow = y + (size_t)row * N + (size_t)tn * BN;
+      const float4* swv = reinterpret_cast<const float4*>(sw + (size_t)tn * BN);
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
+        tc::tmem_ld_wait();
+        uint32_t p[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 s4 = __ldg(swv + c * 8 + j);
+          p[2 * j] = pack_bf16x2(__uint_as_float(v[4 * j]) * srow * s4.x,
+                                 __uint_as_float(v[4 * j + 1]) * srow * s4.y);
+          p[2 * j + 1] = pack_bf16x2(__uint_as_float(v[4 * j + 2]) * srow * s4.z,
+                                     __uint_as_float(v[4 * j + 3]) * srow * s4.w);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->acc_empty[buf]);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                          int M, int N, int K, void* y, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  if (!tc::make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
+                        (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
+                        (uint64_t)K, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return RF_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+      return RF_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = (M / BM) * (N / BN);
+  const int sms = tc::sm_count();
+  const int grid = sms > 0 && sms < tiles ? sms : tiles;
+  fp8_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sx, sw,
+                                                     static_cast<__nv_bfloat16*>(y), M, N, K);
+  return launch_status();
+}
+
+rf_status gemm_take_status(int* status) {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+  *status = v;
+  return RF_OK;
 }
 
 }  // namespace rf

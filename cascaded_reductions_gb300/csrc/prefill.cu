@@ -8,8 +8,7 @@ rf_status launch_prefill(const void*, const void*, const void*, int, int, int, i
   return RF_ERR_UNSUPPORTED;
 }
 
-rf_status read_device_error(int* status, cudaStream_t st) {
-  if (cudaStreamSynchronize(st) != cudaSuccess) return RF_ERR_CUDA;
+rf_status prefill_take_status(int* status) {
   *status = RF_OK;
   return RF_OK;
 }

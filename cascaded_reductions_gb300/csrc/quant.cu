@@ -6,9 +6,17 @@
 // the CTA (warp shuffles, then one shared-memory step), and the same
 // registers are encoded: sx = amax / 448 (IEEE fp32 division), code =
 // e4m3(x / sx) with the hardware's round-to-nearest-even saturating convert.
-// The element step divides by the scale (correctly rounded fp32 quotient)
-// rather than multiplying by a reciprocal, so every code is the one the
-// definition gives.  A row with amax = 0 writes sx = 0 and zero codes.
+// The element step is the correctly rounded fp32 quotient x / sx (not x times
+// a rounded reciprocal, which can flip codes), so every code is the one the
+// definition gives.  The quotient comes from the row's correctly rounded
+// reciprocal r = 1/sx and two residual corrections q' = q + (x - q sx) r, each
+// residual exact in one fma; by Markstein's theorem (P. Markstein, IBM J. Res.
+// Dev. 34(1), 1990: a faithful quotient corrected once with the correctly
+// rounded reciprocal is the correctly rounded quotient) the result equals
+// IEEE division.  Rows whose scale is below 2^-90 use the library's IEEE
+// division instead, so no residual can underflow where it matters (a quotient
+// below 2^-10 encodes to zero whatever its last bits).  A row with amax = 0
+// writes sx = 0 and zero codes.
 // Rows longer than the register budget use a two-pass variant that reads
 // the row a second time (from L2).
 
@@ -33,12 +41,37 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
 }
 
-__device__ __forceinline__ uint2 encode8(const uint4& u, float s, bool zero) {
-  if (zero) return make_uint2(0u, 0u);
-  const uint32_t c0 = e4m3x2(__fdiv_rn(bf16_lo(u.x), s), __fdiv_rn(bf16_hi(u.x), s));
-  const uint32_t c1 = e4m3x2(__fdiv_rn(bf16_lo(u.y), s), __fdiv_rn(bf16_hi(u.y), s));
-  const uint32_t c2 = e4m3x2(__fdiv_rn(bf16_lo(u.z), s), __fdiv_rn(bf16_hi(u.z), s));
-  const uint32_t c3 = e4m3x2(__fdiv_rn(bf16_lo(u.w), s), __fdiv_rn(bf16_hi(u.w), s));
+// Per-row divisor: s, its correctly rounded reciprocal, and which path to use.
+struct Divisor {
+  float s, r;
+  bool exact_path;   // tiny scale: IEEE division for every element
+  bool zero;         // amax == 0: all codes zero
+};
+
+__device__ __forceinline__ Divisor make_divisor(float s) {
+  Divisor d;
+  d.s = s;
+  d.zero = s == 0.f;
+  d.exact_path = s < 0x1p-90f;
+  d.r = d.exact_path ? 0.f : __frcp_rn(s);
+  return d;
+}
+
+// correctly rounded x / s (see the file comment); the sign of a zero x is kept
+__device__ __forceinline__ float quotient(float x, const Divisor& d) {
+  if (d.exact_path) return __fdiv_rn(x, d.s);
+  float q = x * d.r;
+  q = fmaf(fmaf(-q, d.s, x), d.r, q);
+  q = fmaf(fmaf(-q, d.s, x), d.r, q);
+  return copysignf(q, x);
+}
+
+__device__ __forceinline__ uint2 encode8(const uint4& u, const Divisor& d) {
+  if (d.zero) return make_uint2(0u, 0u);
+  const uint32_t c0 = e4m3x2(quotient(bf16_lo(u.x), d), quotient(bf16_hi(u.x), d));
+  const uint32_t c1 = e4m3x2(quotient(bf16_lo(u.y), d), quotient(bf16_hi(u.y), d));
+  const uint32_t c2 = e4m3x2(quotient(bf16_lo(u.z), d), quotient(bf16_hi(u.z), d));
+  const uint32_t c3 = e4m3x2(quotient(bf16_lo(u.w), d), quotient(bf16_hi(u.w), d));
   return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
 }
 
@@ -72,12 +105,12 @@ absmax_quant_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict__ xq,
   }
   const float amax = block_max<THREADS>(a, red);
   const float s = __fdiv_rn(amax, 448.f);
-  const bool zero = amax == 0.f;
+  const Divisor d = make_divisor(s);
   if (threadIdx.x == 0) sx[blockIdx.x] = s;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * THREADS + threadIdx.x;
-    if (c < K8) xq[base + c] = encode8(r[i], s, zero);
+    if (c < K8) xq[base + c] = encode8(r[i], d);
   }
 }
 
@@ -92,9 +125,9 @@ absmax_quant_long_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict_
   for (int c = threadIdx.x; c < K8; c += THREADS) a = absmax8(x[base + c], a);
   const float amax = block_max<THREADS>(a, red);
   const float s = __fdiv_rn(amax, 448.f);
-  const bool zero = amax == 0.f;
+  const Divisor d = make_divisor(s);
   if (threadIdx.x == 0) sx[blockIdx.x] = s;
-  for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8(x[base + c], s, zero);
+  for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8(x[base + c], d);
 }
 
 }  // namespace

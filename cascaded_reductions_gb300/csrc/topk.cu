@@ -5,21 +5,22 @@
 // exp-sum denominator and the k largest entries all come from a single pass
 // over the logits held in registers.
 //
-// Layout: a group of G lanes (G = 32, or 16 for E <= 64 and k <= 16) owns one
-// token; each lane holds NV 16-byte chunks of the row (4*NV logits), loaded
-// with coalesced 16-byte loads (or scalar loads when E % 4 != 0).  Padding
-// slots hold -inf and never win.
-//   1. group max m and sum l = sum exp(x - m) (xor shuffles);
-//   2. k rounds of group arg-max on the raw fp32 logits: each lane proposes
-//      its best untaken slot (larger value, then lower expert index), the
-//      group reduces (value, index) pairs, the owner marks the winner taken,
-//      and lane r of the group keeps round r's winner;
-//   3. lanes r < k turn their winner into a weight exp(x - m) / l, or
-//      exp(x - m) / sum over the selected (renormalised), and store the
-//      k indices and weights with one coalesced store each.
-// Ordering by the raw logits (not by rounded exponentials, which can tie)
-// makes equal probabilities come out in index order exactly when their
-// logits are equal.
+// Layout: one warp owns TPW tokens; lane j holds NV logits of each token,
+// loaded W at a time (W = 4, 2 or 1 consecutive floats, coalesced across the
+// warp).  Each logit is turned into an order-preserving 32-bit key (-0 is
+// first mapped to +0, so keys compare exactly like the float values).
+//   * round r of top-k: every lane proposes its largest untaken key (slots
+//     are scanned in increasing expert index, so among equal keys the lowest
+//     index is proposed); the warp takes the maximum key with one
+//     redux.sync, then the minimum expert index among the lanes proposing
+//     that key with a second redux.sync; the owner marks it taken and lane r
+//     keeps it.  Equal logits therefore come out in index order;
+//   * the row max m is round 0's key; with renormalisation the weights are
+//     exp(x_i - m) / sum over the k selected, otherwise exp(x_i - m) / l with
+//     l = sum over all E of exp(x - m);
+//   * lanes r < k store index and weight with one coalesced store each.
+// The TPW tokens of a warp are processed side by side so their loads and
+// reduction chains overlap.
 
 #include <math.h>
 
@@ -28,129 +29,152 @@
 namespace rf {
 namespace {
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
+constexpr uint32_t FULL = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x + 0.0f);     // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int G, int NV, bool VEC>
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// NV logits per lane (E <= 32*NV), W consecutive logits per load, TPW tokens
+// per warp.  Padding slots get key 0, below every real key.
+template <int NV, int W, int TPW>
 __global__ void __launch_bounds__(256)
 softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renorm,
                     int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
-  constexpr int NVAL = 4 * NV;   // values per lane
-  static_assert(NVAL <= 32, "taken mask is 32 bits");
+  static_assert(NV % W == 0 && NV <= 32, "layout");
   const int lane = threadIdx.x & 31;
-  const int j = lane & (G - 1);                 // lane within the group
-  const int token = (blockIdx.x * 256 + threadIdx.x) / G;
-  // All lanes of a warp take part in the shuffles; groups past the end run
-  // with all slots at -inf and store nothing.
-  const bool live = token < T;
-  const float* row = logits + (size_t)(live ? token : 0) * E;
+  const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int tok0 = warp_id * TPW;
 
-  float x[NVAL];
+  uint32_t key[TPW][NV];
 #pragma unroll
-  for (int v = 0; v < NV; ++v) {
-    if (VEC) {
-      const int e0 = (v * G + j) * 4;
-      if (live && e0 < E) {
-        const float4 f = __ldcs(reinterpret_cast<const float4*>(row + e0));
-        x[4 * v + 0] = f.x; x[4 * v + 1] = f.y; x[4 * v + 2] = f.z; x[4 * v + 3] = f.w;
+  for (int t = 0; t < TPW; ++t) {
+    const int token = tok0 + t;
+    const bool live = token < T;
+    const float* row = logits + (size_t)(live ? token : 0) * E;
+#pragma unroll
+    for (int c = 0; c < NV / W; ++c) {
+      const int e0 = c * 32 * W + lane * W;
+      if (W == 4) {
+        if (live && e0 < E) {
+          const float4 f = __ldcs(reinterpret_cast<const float4*>(row + e0));
+          key[t][4 * c + 0] = order_key(f.x);
+          key[t][4 * c + 1] = order_key(f.y);
+          key[t][4 * c + 2] = order_key(f.z);
+          key[t][4 * c + 3] = order_key(f.w);
+        } else {
+#pragma unroll
+          for (int w = 0; w < W; ++w) key[t][W * c + w] = 0u;
+        }
+      } else if (W == 2) {
+        if (live && e0 < E) {
+          const float2 f = __ldcs(reinterpret_cast<const float2*>(row + e0));
+          key[t][2 * c + 0] = order_key(f.x);
+          key[t][2 * c + 1] = order_key(f.y);
+        } else {
+          key[t][2 * c + 0] = key[t][2 * c + 1] = 0u;
+        }
       } else {
-        x[4 * v + 0] = x[4 * v + 1] = x[4 * v + 2] = x[4 * v + 3] = -INFINITY;
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int e = (4 * v + t) * G + j;
-        x[4 * v + t] = (live && e < E) ? __ldcs(row + e) : -INFINITY;
+        key[t][c] = (live && e0 < E) ? order_key(__ldcs(row + e0)) : 0u;
       }
     }
   }
   // expert index of slot i of this lane
-  auto slot_index = [&](int i) -> int {
-    return VEC ? ((i >> 2) * G + j) * 4 + (i & 3) : i * G + j;
-  };
+  auto expert = [&](int i) -> int { return (i / W) * 32 * W + lane * W + (i % W); };
 
-  // reduction 1: max; reduction 2: sum of exp(x - m)
-  float m = -INFINITY;
+  uint32_t taken[TPW];
+  uint32_t mykey[TPW];
+  int myidx[TPW];
 #pragma unroll
-  for (int i = 0; i < NVAL; ++i) m = fmaxf(m, x[i]);
-  m = group_max<G>(m);
-  const float mref = m == -INFINITY ? 0.f : m;
-  float l = 0.f;
-#pragma unroll
-  for (int i = 0; i < NVAL; ++i) l += expf(x[i] - mref);
-  l = group_sum<G>(l);
+  for (int t = 0; t < TPW; ++t) {
+    taken[t] = 0u;
+    mykey[t] = 0u;
+    myidx[t] = 0;
+  }
 
-  // top-k rounds
-  uint32_t taken = 0;
-  float my_val = -INFINITY;
-  int my_idx = 0x7fffffff;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    int bslot = -1;
 #pragma unroll
-    for (int i = 0; i < NVAL; ++i) {
-      const int e = slot_index(i);
-      if (!((taken >> i) & 1u) && e < E && better(x[i], e, bv, bi)) {
-        bv = x[i];
-        bi = e;
-        bslot = i;
-      }
-    }
-    float gv = bv;
-    int gi = bi;
+    for (int t = 0; t < TPW; ++t) {
+      uint32_t bk = 0u;
+      int bs = -1;
 #pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, gv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, gi, o);
-      if (better(ov, oi, gv, gi)) {
-        gv = ov;
-        gi = oi;
+      for (int i = 0; i < NV; ++i) {
+        if (!((taken[t] >> i) & 1u) && key[t][i] > bk) {
+          bk = key[t][i];
+          bs = i;
+        }
       }
-    }
-    if (bslot >= 0 && bi == gi) taken |= 1u << bslot;
-    if (j == r) {
-      my_val = gv;
-      my_idx = gi;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (i == bs) bi = expert(i);
+      const uint32_t gk = __reduce_max_sync(FULL, bk);
+      const int gi = (int)__reduce_min_sync(FULL, bk == gk ? (uint32_t)bi : 0x7fffffffu);
+      if (bs >= 0 && bk == gk && bi == gi) taken[t] |= 1u << bs;
+      if (lane == r) {
+        mykey[t] = gk;
+        myidx[t] = gi;
+      }
     }
   }
 
-  float w = (j < k) ? expf(my_val - mref) : 0.f;
-  float denom = l;
-  if (renorm) denom = group_sum<G>(w);
-  if (live && j < k) {
-    idx_out[(size_t)token * k + j] = my_idx;
-    w_out[(size_t)token * k + j] = w / denom;
+#pragma unroll
+  for (int t = 0; t < TPW; ++t) {
+    const int token = tok0 + t;
+    const float m = key_value(__shfl_sync(FULL, mykey[t], 0));   // round 0 = row max
+    const float w = lane < k ? expf(key_value(mykey[t]) - m) : 0.f;
+    float denom;
+    if (renorm) {
+      denom = group_sum<32>(w);
+    } else {
+      float l = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (key[t][i] != 0u) l += expf(key_value(key[t][i]) - m);
+      denom = group_sum<32>(l);
+    }
+    if (token < T && lane < k) {
+      idx_out[(size_t)token * k + lane] = myidx[t];
+      w_out[(size_t)token * k + lane] = w / denom;
+    }
   }
 }
 
-template <int G, int NV>
+template <int NV, int W, int TPW>
 void launch_one(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
                 cudaStream_t st) {
-  const int tokens_per_block = 256 / G;
-  const unsigned grid = (unsigned)((T + tokens_per_block - 1) / tokens_per_block);
-  if (E % 4 == 0)
-    softmax_topk_kernel<G, NV, true><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
-  else
-    softmax_topk_kernel<G, NV, false><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
+  const int warps = (T + TPW - 1) / TPW;
+  const unsigned grid = (unsigned)((warps + 7) / 8);
+  softmax_topk_kernel<NV, W, TPW><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
 }
 
 }  // namespace
 
 rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int renormalize,
                               int32_t* idx, float* w, cudaStream_t st) {
-  // lanes r < k hold round r's winner, so a group needs at least k lanes
-  if (E <= 64 && k <= 16) {
-    launch_one<16, 1>(logits, T, E, k, renormalize, idx, w, st);
+  const bool v4 = E % 4 == 0, v2 = E % 2 == 0;
+  if (E <= 32) {
+    launch_one<1, 1, 4>(logits, T, E, k, renormalize, idx, w, st);
+  } else if (E <= 64) {
+    if (v2) launch_one<2, 2, 4>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_one<2, 1, 4>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 128) {
-    launch_one<32, 1>(logits, T, E, k, renormalize, idx, w, st);
+    if (v4) launch_one<4, 4, 2>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_one<4, 1, 2>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 256) {
-    launch_one<32, 2>(logits, T, E, k, renormalize, idx, w, st);
+    if (v4) launch_one<8, 4, 2>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_one<8, 1, 2>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 512) {
-    launch_one<32, 4>(logits, T, E, k, renormalize, idx, w, st);
+    if (v4) launch_one<16, 4, 1>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_one<16, 1, 1>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 1024) {
-    launch_one<32, 8>(logits, T, E, k, renormalize, idx, w, st);
+    if (v4) launch_one<32, 4, 1>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_one<32, 1, 1>(logits, T, E, k, renormalize, idx, w, st);
   } else {
     return RF_ERR_UNSUPPORTED;
   }

@@ -97,7 +97,7 @@ rf_status rf_attn_decode_split(const void* q, const void* k, const void* v,
  *   out        [R, D]       out_dtype out (RF_F32 or RF_BF16, round to nearest even)
  *   lse        [R]          fp32 out, may be NULL
  * Errors: RF_ERR_INVALID_ARG for null inputs/out, R, S, D <= 0;
- * RF_ERR_UNSUPPORTED for D not in {64, 128} or S > 1024.
+ * RF_ERR_UNSUPPORTED for D not in {64, 128}.
  * A row whose S states are all identity states gives NaN (it had no keys).
  */
 rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc,

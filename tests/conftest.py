@@ -8,6 +8,22 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def load_builder():
+    """cascaded_reductions_gb300/_build.py loaded by path (the package's
+    __init__ needs the library it builds)."""
+    import importlib.util
+    path = os.path.join(ROOT, "cascaded_reductions_gb300", "_build.py")
+    spec = importlib.util.spec_from_file_location("rf_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def pytest_sessionstart(session):
+    # nvcc is present wherever the tests run; a no-op when librf.so is current
+    load_builder().build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
 

@@ -81,3 +81,40 @@ def test_zero_row_grid_rows_and_signed_zero(rf):
     assert gs[0] == 0 and np.all(gq[0] == 0)
     assert gs[1] == 1.0
     assert np.all(gq[2][5:] == 0x80)
+
+
+def test_quotients_across_every_binade(rf):
+    """Rows whose quotients x / sx sweep every e4m3 binade with all bf16
+    mantissas, for 48 unrelated scales: exercises the correctly rounded
+    quotient near every e4m3 rounding boundary."""
+    g = torch.Generator().manual_seed(21)
+    rows = []
+    mant = torch.arange(128, dtype=torch.float64) / 128.0 + 1.0
+    for r in range(48):
+        amax = float(torch.empty(1).uniform_(-8, 8, generator=g).exp2())
+        s = amax / 448.0
+        vals = torch.cat([s * (2.0 ** j) * mant for j in range(-12, 8)])
+        sign = torch.where(torch.rand(vals.shape, generator=g) < 0.5, -1.0, 1.0)
+        row = torch.cat([torch.tensor([amax], dtype=torch.float64), vals * sign])
+        rows.append(row[:2560])
+    x = torch.stack(rows).to(torch.bfloat16)
+    check(rf, x, "binade sweep")
+
+
+def test_exact_midpoints_round_to_even(rf):
+    """Scale an exact power of two (amax = 448 * 2^p): every e4m3 midpoint
+    and its bf16 neighbours land exactly where the encoder must break ties."""
+    codes = torch.arange(0, 0x7D, dtype=torch.uint8)      # neighbours stay below 448
+    lo = codes.view(torch.float8_e4m3fn).double()
+    hi = (codes + 1).view(torch.float8_e4m3fn).double()
+    mid = (lo + hi) / 2
+    base = torch.cat([mid, lo, hi, -mid, -lo])
+    rows = []
+    for p in (-6, -1, 0, 3, 9):
+        row = torch.cat([torch.tensor([448.0]), base]) * 2.0 ** p
+        row = row.to(torch.bfloat16)
+        nxt = row.view(torch.int16) + 1              # the bf16 neighbour above each value
+        rows.append(torch.cat([row, nxt.view(torch.bfloat16)[1:]]))
+    n = min(r.numel() for r in rows) // 8 * 8
+    x = torch.stack([r[:n] for r in rows])
+    check(rf, x, "midpoints")

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "rf_absmax_quant_e4m3": (_I, [_P, _I, _I, _P, _P, _P]),
     "rf_fp8_gemm_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "rf_device_error": (_I, [ctypes.POINTER(_I), _P]),
+    "rf_attn_decode_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P]),
 }
 
 
@@ -191,6 +192,25 @@ def rf_absmax_quant_fp8_gemm(x, wq, sw, xq, sx, y, stream=None):
     _need(y, torch.bfloat16, "y", (M, N))
     _check(_lib.rf_absmax_quant_fp8_gemm(_ptr(x), M, K, _ptr(wq), _ptr(sw), N, _ptr(xq), _ptr(sx),
                                          _ptr(y), _stream(stream)), "rf_absmax_quant_fp8_gemm")
+
+
+def rf_attn_decode_noalloc(q, k, v, S, scale, out, lse=None, stream=None):
+    """Decode split + merge with the segment states in the library's fixed
+    16 MiB device array: for callers that cannot allocate device memory.
+
+    q [R, D], k/v [R, L, D] (fp32 D=64 or bf16 D=128); out [R, D] fp32 or
+    bf16; lse [R] fp32 (optional).  Calls that may overlap on the GPU share the
+    array and race; the first call on a device must precede stream capture."""
+    R, L, D = k.shape
+    _need(q, k.dtype, "q", (R, D))
+    _need(k, k.dtype, "k")
+    _need(v, k.dtype, "v", (R, L, D))
+    _need(out, out.dtype, "out", (R, D))
+    if lse is not None:
+        _need(lse, torch.float32, "lse", (R,))
+    _check(_lib.rf_attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale),
+                                       _dtype_code(k.dtype), _ptr(out), _dtype_code(out.dtype),
+                                       _ptr(lse), _stream(stream)), "rf_attn_decode_noalloc")
 
 
 def rf_device_error(stream=None):

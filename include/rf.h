@@ -164,6 +164,34 @@ rf_status rf_absmax_quant_fp8_gemm(const void* x, int M, int K,
                                    const uint8_t* wq, const float* sw, int N,
                                    uint8_t* xq, float* sx, void* y, void* stream);
 
+/*
+ * rf_attn_decode_noalloc -- rf_attn_decode_split followed by rf_state_merge
+ * for callers that cannot allocate device memory: for example a plugin inside
+ * a host engine that owns every device allocation, a latency-critical loop
+ * that cannot afford cudaMalloc's implicit device synchronisation, or a
+ * process whose memory budget was fixed at start-up.  The pages have no
+ * counterpart to this call; it is a deployment convenience.
+ *
+ * Same q, k, v, R, L, D, S, scale, dtype as rf_attn_decode_split and same
+ * out, out_dtype, lse as rf_state_merge.  The segment states live in a fixed
+ * 16 MiB array inside the library (allocated once per GPU when the library
+ * is loaded, kept until the process exits) instead of caller buffers, so the
+ * call itself allocates nothing.
+ * - It needs 8*R*S bytes rounded up to 256, plus 4*R*S*D bytes, to fit in
+ *   16 MiB; larger requests return RF_ERR_UNSUPPORTED with nothing launched.
+ * - Every call on a GPU shares that array: calls that may overlap on the GPU
+ *   (different streams, unordered host threads) race; order them on one
+ *   stream.  Each call rewrites every state it reads, so nothing needs
+ *   clearing between calls.
+ * - The first call on each device (with that device current) looks up the
+ *   array's device address; make it before any stream capture.
+ * Errors: as rf_attn_decode_split and rf_state_merge; RF_ERR_CUDA if the
+ * address look-up fails.
+ */
+rf_status rf_attn_decode_noalloc(const void* q, const void* k, const void* v,
+                                 int R, int L, int D, int S, float scale, int dtype,
+                                 void* out, int out_dtype, float* lse, void* stream);
+
 /* Phase 1 of rf_absmax_quant_fp8_gemm alone (same arguments and rules;
  * any K % 8 == 0 is supported). */
 rf_status rf_absmax_quant_e4m3(const void* x, int M, int K, uint8_t* xq, float* sx,

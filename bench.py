@@ -363,6 +363,16 @@ def run_rf(args):
     import synthetic_inputs as si
 
     peaks = measured_peaks()
+    if args.only:
+        # one cascade alone (used for profiler captures of a single kernel)
+        fns = {"single_row": lambda: path_single_row(torch, rf, peaks),
+               "routing_256": lambda: path_routing(torch, rf, peaks, "route_256"),
+               "routing_64": lambda: path_routing(torch, rf, peaks, "route_64"),
+               "quant": lambda: path_quant(torch, rf, peaks),
+               "gemm": lambda: path_gemm(torch, rf, peaks),
+               "prefill": lambda: path_prefill(torch, rf, peaks)}
+        print(json.dumps({args.only: fns[args.only]()}), flush=True)
+        return
     B, H, L, D = DECODE["B"], DECODE["H"], DECODE["L"], DECODE["D"]
     if args.rows:                      # smaller batch of rows (profiling captures)
         B, H = 1, args.rows
@@ -539,6 +549,8 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="decode rows instead of B*H=1024 (small cases for ncu captures)")
     ap.add_argument("--decode-only", action="store_true", help="skip the other cascades")
+    ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm",
+                                       "prefill"], help="time one other cascade alone")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work")

@@ -28,12 +28,20 @@
 namespace rf {
 namespace {
 
-__device__ __forceinline__ float absmax8(const uint4& u, float a) {
-  a = fmaxf(a, fabsf(bf16_lo(u.x))); a = fmaxf(a, fabsf(bf16_hi(u.x)));
-  a = fmaxf(a, fabsf(bf16_lo(u.y))); a = fmaxf(a, fabsf(bf16_hi(u.y)));
-  a = fmaxf(a, fabsf(bf16_lo(u.z))); a = fmaxf(a, fabsf(bf16_hi(u.z)));
-  a = fmaxf(a, fabsf(bf16_lo(u.w))); a = fmaxf(a, fabsf(bf16_hi(u.w)));
-  return a;
+// running |x| maximum of 8 bf16 values, kept as a packed bf16x2 pair
+// (the maximum of bf16 magnitudes is exact in bf16)
+__device__ __forceinline__ uint32_t absmax8(const uint4& u, uint32_t a) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(u.x & m), "r"(u.y & m));
+  asm("max.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(u.z & m));
+  asm("max.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(u.w & m));
+  asm("max.bf16x2 %0, %0, %1;" : "+r"(r) : "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ float absmax_value(uint32_t pair) {
+  return fmaxf(bf16_lo(pair), bf16_hi(pair));
 }
 
 // two floats -> two e4m3 codes (x0 in the low byte), RNE, saturating
@@ -41,39 +49,35 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Per-row divisor: s, its correctly rounded reciprocal, and which path to use.
-struct Divisor {
-  float s, r;
-  bool exact_path;   // tiny scale: IEEE division for every element
-  bool zero;         // amax == 0: all codes zero
-};
-
-__device__ __forceinline__ Divisor make_divisor(float s) {
-  Divisor d;
-  d.s = s;
-  d.zero = s == 0.f;
-  d.exact_path = s < 0x1p-90f;
-  d.r = d.exact_path ? 0.f : __frcp_rn(s);
-  return d;
-}
-
-// correctly rounded x / s (see the file comment); the sign of a zero x is kept
-__device__ __forceinline__ float quotient(float x, const Divisor& d) {
-  if (d.exact_path) return __fdiv_rn(x, d.s);
-  float q = x * d.r;
-  q = fmaf(fmaf(-q, d.s, x), d.r, q);
-  q = fmaf(fmaf(-q, d.s, x), d.r, q);
+// correctly rounded x / s from r = RN(1/s) (see the file comment); the sign
+// of a zero x is kept
+__device__ __forceinline__ float quotient(float x, float s, float r) {
+  float q = x * r;
+  q = fmaf(fmaf(-q, s, x), r, q);
+  q = fmaf(fmaf(-q, s, x), r, q);
   return copysignf(q, x);
 }
 
-__device__ __forceinline__ uint2 encode8(const uint4& u, const Divisor& d) {
-  if (d.zero) return make_uint2(0u, 0u);
-  const uint32_t c0 = e4m3x2(quotient(bf16_lo(u.x), d), quotient(bf16_hi(u.x), d));
-  const uint32_t c1 = e4m3x2(quotient(bf16_lo(u.y), d), quotient(bf16_hi(u.y), d));
-  const uint32_t c2 = e4m3x2(quotient(bf16_lo(u.z), d), quotient(bf16_hi(u.z), d));
-  const uint32_t c3 = e4m3x2(quotient(bf16_lo(u.w), d), quotient(bf16_hi(u.w), d));
+__device__ __forceinline__ uint2 encode8(const uint4& u, float s, float r) {
+  const uint32_t c0 = e4m3x2(quotient(bf16_lo(u.x), s, r), quotient(bf16_hi(u.x), s, r));
+  const uint32_t c1 = e4m3x2(quotient(bf16_lo(u.y), s, r), quotient(bf16_hi(u.y), s, r));
+  const uint32_t c2 = e4m3x2(quotient(bf16_lo(u.z), s, r), quotient(bf16_hi(u.z), s, r));
+  const uint32_t c3 = e4m3x2(quotient(bf16_lo(u.w), s, r), quotient(bf16_hi(u.w), s, r));
   return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
 }
+
+// rows with a tiny (or zero) scale: IEEE division per element, or zero codes
+__device__ __noinline__ uint2 encode8_exact(uint4 u, float s) {
+  if (s == 0.f) return make_uint2(0u, 0u);
+  const uint32_t c0 = e4m3x2(__fdiv_rn(bf16_lo(u.x), s), __fdiv_rn(bf16_hi(u.x), s));
+  const uint32_t c1 = e4m3x2(__fdiv_rn(bf16_lo(u.y), s), __fdiv_rn(bf16_hi(u.y), s));
+  const uint32_t c2 = e4m3x2(__fdiv_rn(bf16_lo(u.z), s), __fdiv_rn(bf16_hi(u.z), s));
+  const uint32_t c3 = e4m3x2(__fdiv_rn(bf16_lo(u.w), s), __fdiv_rn(bf16_hi(u.w), s));
+  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
+}
+
+// the reciprocal-and-correction path is valid for scales of 2^-90 and up
+__device__ __forceinline__ bool fast_scale(float s) { return s >= 0x1p-90f; }
 
 template <int THREADS>
 __device__ __forceinline__ float block_max(float a, float* red) {
@@ -93,24 +97,32 @@ absmax_quant_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict__ xq,
                     float* __restrict__ sx) {
   __shared__ float red[THREADS / 32];
   const size_t base = (size_t)blockIdx.x * K8;
-  uint4 r[VPT];
-  float a = 0.f;
+  uint4 v[VPT];
+  uint32_t a = 0u;
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * THREADS + threadIdx.x;
     if (c < K8) {
-      r[i] = ld_stream_v4(x + base + c);
-      a = absmax8(r[i], a);
+      v[i] = ld_stream_v4(x + base + c);
+      a = absmax8(v[i], a);
     }
   }
-  const float amax = block_max<THREADS>(a, red);
+  const float amax = block_max<THREADS>(absmax_value(a), red);
   const float s = __fdiv_rn(amax, 448.f);
-  const Divisor d = make_divisor(s);
   if (threadIdx.x == 0) sx[blockIdx.x] = s;
+  if (fast_scale(s)) {
+    const float r = __frcp_rn(s);
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int c = i * THREADS + threadIdx.x;
-    if (c < K8) xq[base + c] = encode8(r[i], d);
+    for (int i = 0; i < VPT; ++i) {
+      const int c = i * THREADS + threadIdx.x;
+      if (c < K8) xq[base + c] = encode8(v[i], s, r);
+    }
+  } else {
+#pragma unroll 1
+    for (int i = 0; i < VPT; ++i) {
+      const int c = i * THREADS + threadIdx.x;
+      if (c < K8) xq[base + c] = encode8_exact(v[i], s);
+    }
   }
 }
 
@@ -121,13 +133,17 @@ absmax_quant_long_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict_
                          float* __restrict__ sx) {
   __shared__ float red[THREADS / 32];
   const size_t base = (size_t)blockIdx.x * K8;
-  float a = 0.f;
+  uint32_t a = 0u;
   for (int c = threadIdx.x; c < K8; c += THREADS) a = absmax8(x[base + c], a);
-  const float amax = block_max<THREADS>(a, red);
+  const float amax = block_max<THREADS>(absmax_value(a), red);
   const float s = __fdiv_rn(amax, 448.f);
-  const Divisor d = make_divisor(s);
   if (threadIdx.x == 0) sx[blockIdx.x] = s;
-  for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8(x[base + c], d);
+  if (fast_scale(s)) {
+    const float r = __frcp_rn(s);
+    for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8(x[base + c], s, r);
+  } else {
+    for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8_exact(x[base + c], s);
+  }
 }
 
 }  // namespace

@@ -6,7 +6,8 @@
 // running state per row; the state lives at the block level of the reduction
 // tree (cue 31), one thread per query row.
 //
-// One CTA per (batch*head, 128-row query tile), heaviest causal tiles first.
+// One CTA per (batch*head, 128-row query tile), head-major, heaviest causal
+// tile of each head first.
 //   warp 4      TMA: Q tile once, then K_j and V_j tiles (two 64-column
 //               boxes each, 128-byte swizzle) into a 2-stage ring;
 //   warp 5      allocates 512 TMEM columns and issues the MMAs from one
@@ -88,9 +89,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int NB = N / BM;
-  // heaviest causal tiles first: the first wave takes the last query tiles
-  const int mblk = NB - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
+  // head-major order, heaviest causal tile of each head first: the CTAs that
+  // run at the same time share a head's K and V through L2
+  const int bh = (int)(blockIdx.x / NB);
+  const int mblk = NB - 1 - (int)(blockIdx.x % NB);
   const int nblocks = causal ? mblk + 1 : NB;
   const int row0 = bh * N + mblk * BM;        // first global row of this Q tile
   const int key0 = bh * N;
@@ -202,16 +204,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tc::tmem_ld_32x32b_x32(lane_base + s_col(j) + (uint32_t)(c * 32), v);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]) * scale_log2;
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
       if (causal && j == mblk) {
 #pragma unroll
         for (int i = 0; i < BN; ++i)
           if (i > r) s[i] = -INFINITY;
       }
+      // raw scores here; scale_log2 > 0 is applied inside the exponent
       float mt = -INFINITY;
 #pragma unroll
       for (int i = 0; i < BN; ++i) mt = fmaxf(mt, s[i]);
+      mt *= scale_log2;
       // move the reference max only when it has grown by more than the threshold
       const bool move = mt > m_ref + RESCALE_THRESHOLD;
       const float m_new = move ? mt : m_ref;
@@ -224,8 +228,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(s[c * 32 + 2 * i] - m_new);
-          const float p1 = ex2(s[c * 32 + 2 * i + 1] - m_new);
+          const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, -m_new));
+          const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, -m_new));
           rowsum += p0 + p1;
           w[i] = pack_bf16x2(p0, p1);
         }

@@ -46,6 +46,7 @@ struct Shared {
 };
 
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(Shared) + 1024;
+static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB of shared memory a CTA may use");
 
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

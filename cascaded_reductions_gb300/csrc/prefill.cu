@@ -8,19 +8,20 @@
 //
 // One CTA per (batch*head, 128-row query tile), head-major, heaviest causal
 // tile of each head first.
-//   warp 4      TMA: Q tile once, then K_j and V_j tiles (two 64-column
-//               boxes each, 128-byte swizzle) into a 2-stage ring;
-//   warp 5      allocates 512 TMEM columns and issues the MMAs from one
+//   warp 8      TMA: Q tile once, then K_j and V_j tiles (two 64-column
+//               boxes each, 128-byte swizzle) into a 3-stage ring;
+//   warp 9      allocates 512 TMEM columns and issues the MMAs from one
 //               thread: S_j = Q K_j^T (kind::f16, 128x128x16, both operands
 //               K-major in shared memory) into one of two S buffers, and
 //               O += P_j V_j with P_j read from TMEM (it overwrites the first
 //               64 columns of S_j as bf16 pairs) and V_j MN-major in shared
 //               memory.  S_{j+1} is issued before P_j is ready, so the tensor
 //               core computes the next scores while the softmax runs;
-//   warps 0-3   softmax, one thread per query row (TMEM lane): load S_j,
-//               mask the diagonal tile, running max in the log2 domain
-//               (scores times scale*log2(e)), p = exp2(s - m_ref), row sum,
-//               P_j back to TMEM; then the epilogue out = O / l, lse.
+//   warps 0-7   softmax, two threads per query row (TMEM lane), one per
+//               64-key half: load S_j, mask the diagonal tile, tile max in
+//               the log2 domain (scores times scale*log2(e)), p = exp2(s -
+//               m_ref), partial row sum, P_j back to TMEM; then the epilogue
+//               out = O / l (l = the two partial sums), lse.
 // Rescaling is lazy: the reference max m_ref of a row moves (and O and l are
 // multiplied by exp2(m_ref_old - m_ref_new)) only when the tile max exceeds
 // it by more than 8, so p <= 2^8.  The result is the same mathematics (O and
@@ -37,10 +38,10 @@ namespace {
 constexpr int BM = 128;            // query rows per tile
 constexpr int BN = 128;            // keys per tile
 constexpr int HD = 128;            // head dim
-constexpr int STAGES = 2;
+constexpr int STAGES = 3;
 constexpr int TILE_BYTES = BM * HD * 2;      // 32 KiB (two 16 KiB swizzled halves)
 constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t O_COL = 256;           // S buffers at columns 0 and 128
 __device__ __forceinline__ uint32_t s_col(int j) { return (uint32_t)(j & 1) * 128u; }
@@ -54,12 +55,15 @@ struct Shared {
   uint64_t s_full[2];
   uint64_t p_ready[2];
   uint64_t o_done;
+  uint64_t l_ready;
+  float l_part[2][BM];
   uint32_t tmem_base;
   int abort;
 };
 
 // layout: Q | K[STAGES] | V[STAGES] | Shared
 constexpr size_t SMEM_BYTES = (size_t)(1 + 2 * STAGES) * TILE_BYTES + sizeof(Shared) + 1024;
+static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB of shared memory a CTA may use");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -106,20 +110,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&sh->s_full[b], 1);
-      tc::mbar_init(&sh->p_ready[b], 4);
+      tc::mbar_init(&sh->p_ready[b], 8);
     }
     tc::mbar_init(&sh->o_done, 1);
+    tc::mbar_init(&sh->l_ready, 8);
     sh->abort = 0;
     tc::fence_barrier_init();
   }
-  if (warp == 5) tc::tmem_alloc(&sh->tmem_base, TMEM_COLS);
+  if (warp == 9) tc::tmem_alloc(&sh->tmem_base, TMEM_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
   volatile int* abort = &sh->abort;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------ TMA ----
     if (lane == 0) {
       tc::prefetch_tmap(&tmQ);
@@ -137,7 +142,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         load_tile(sV + s * TILE_BYTES, &tmV, &sh->v_full[s], key0 + j * BN);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------ MMA ----
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(BM, BN, false);
@@ -187,8 +192,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else {
     // --------------------------------------------------- softmax ----
-    const int r = warp * 32 + lane;                 // query row in the tile (TMEM lane)
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // warp w: TMEM lane quarter w & 3 (query rows), column half w >> 2.  Both
+    // threads of a row read all 128 scores of S_j and compute the same tile
+    // max (same values, same order), then each exponentiates its own 64 keys
+    // and, later, rescales and stores its own 64 columns of O.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int r = quarter * 32 + lane;              // query row in the tile (TMEM lane)
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int col0 = half * 64;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nblocks && ok; ++j) {
@@ -197,45 +208,68 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         break;
       }
       tc::fence_after_sync();
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(lane_base + s_col(j) + (uint32_t)(c * 32), v);
+      // own 64 keys (columns col0..col0+63) and the other half's 64
+      float so[64], sx[64];
+      {
+        uint32_t v0[32], v1[32], v2[32], v3[32];
+        const uint32_t sb = lane_base + s_col(j);
+        tc::tmem_ld_32x32b_x32(sb + (uint32_t)col0, v0);
+        tc::tmem_ld_32x32b_x32(sb + (uint32_t)col0 + 32u, v1);
+        tc::tmem_ld_32x32b_x32(sb + (uint32_t)(64 - col0), v2);
+        tc::tmem_ld_32x32b_x32(sb + (uint32_t)(64 - col0) + 32u, v3);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        for (int i = 0; i < 32; ++i) {
+          so[i] = __uint_as_float(v0[i]);
+          so[32 + i] = __uint_as_float(v1[i]);
+          sx[i] = __uint_as_float(v2[i]);
+          sx[32 + i] = __uint_as_float(v3[i]);
+        }
       }
       if (causal && j == mblk) {
+        // key index of so[i] is col0 + i, of sx[i] is (64 - col0) + i
 #pragma unroll
-        for (int i = 0; i < BN; ++i)
-          if (i > r) s[i] = -INFINITY;
+        for (int i = 0; i < 64; ++i) {
+          if (col0 + i > r) so[i] = -INFINITY;
+          if (64 - col0 + i > r) sx[i] = -INFINITY;
+        }
       }
-      // raw scores here; scale_log2 > 0 is applied inside the exponent
-      float mt = -INFINITY;
+      // raw scores here; scale_log2 > 0 is applied inside the exponent.
+      // Independent maxima shorten the dependency chain; both threads of a
+      // row reduce the same 128 values in the same order, so they agree.
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (half == 0) {
 #pragma unroll
-      for (int i = 0; i < BN; ++i) mt = fmaxf(mt, s[i]);
-      mt *= scale_log2;
+        for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], so[i]);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], sx[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], sx[i]);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], so[i]);
+      }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
       // move the reference max only when it has grown by more than the threshold
       const bool move = mt > m_ref + RESCALE_THRESHOLD;
       const float m_new = move ? mt : m_ref;
       const float alpha = ex2(m_ref - m_new);       // 0 on the first tile, 1 when not moved
       l *= alpha;
-      // P_j over the first 64 columns of S_j (two bf16 per column), 16 columns at a time
-      float rowsum = 0.f;
+      // this thread's 64 keys of P_j into its 32 columns of S_j (two bf16 per column)
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, -m_new));
-          const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, -m_new));
-          rowsum += p0 + p1;
+          const float p0 = ex2(fmaf(so[c * 32 + 2 * i], scale_log2, -m_new));
+          const float p1 = ex2(fmaf(so[c * 32 + 2 * i + 1], scale_log2, -m_new));
+          sum[i & 3] += p0 + p1;
           w[i] = pack_bf16x2(p0, p1);
         }
-        tc::tmem_st_32x32b_x16(lane_base + s_col(j) + (uint32_t)(c * 16), w);
+        tc::tmem_st_32x32b_x16(lane_base + s_col(j) + (uint32_t)(half * 32 + c * 16), w);
       }
-      l += rowsum;
+      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       m_ref = m_new;
       // O must hold every earlier P V before it is rescaled
       if (j > 0) {
@@ -246,9 +280,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, move)) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t oc = lane_base + O_COL + (uint32_t)(col0 + c * 32);
             uint32_t v[32];
-            tc::tmem_ld_32x32b_x32(lane_base + O_COL + (uint32_t)(c * 32), v);
+            tc::tmem_ld_32x32b_x32(oc, v);
             tc::tmem_ld_wait();
             uint32_t w0[16], w1[16];
 #pragma unroll
@@ -256,8 +291,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
               w0[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
               w1[i] = __float_as_uint(__uint_as_float(v[16 + i]) * alpha);
             }
-            tc::tmem_st_32x32b_x16(lane_base + O_COL + (uint32_t)(c * 32), w0);
-            tc::tmem_st_32x32b_x16(lane_base + O_COL + (uint32_t)(c * 32 + 16), w1);
+            tc::tmem_st_32x32b_x16(oc, w0);
+            tc::tmem_st_32x32b_x16(oc + 16u, w1);
           }
         }
       }
@@ -266,15 +301,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->p_ready[j & 1]);
     }
+    // the two halves of each row add their partial sums
+    sh->l_part[half][r] = l;
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&sh->l_ready);
     // epilogue: out = O / l, lse = (m_ref + log2 l) * ln 2
-    if (ok && tc::mbar_wait(&sh->o_done, (uint32_t)(nblocks - 1) & 1u, abort)) {
+    if (ok && tc::mbar_wait(&sh->l_ready, 0, abort) &&
+        tc::mbar_wait(&sh->o_done, (uint32_t)(nblocks - 1) & 1u, abort)) {
       tc::fence_after_sync();
-      const float inv = 1.f / l;
-      __nv_bfloat16* orow = out + (size_t)(row0 + r) * HD;
+      const float lt = sh->l_part[0][r] + sh->l_part[1][r];
+      const float inv = 1.f / lt;
+      __nv_bfloat16* orow = out + (size_t)(row0 + r) * HD + col0;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(lane_base + O_COL + (uint32_t)(c * 32), v);
+        tc::tmem_ld_32x32b_x32(lane_base + O_COL + (uint32_t)(col0 + c * 32), v);
         tc::tmem_ld_wait();
         uint32_t pkd[16];
 #pragma unroll
@@ -284,13 +325,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
-      if (lse != nullptr) lse[row0 + r] = (m_ref + log2f(l)) * kLn2;
+      if (lse != nullptr && half == 0) lse[row0 + r] = (m_ref + log2f(lt)) * kLn2;
     }
   }
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -9,12 +9,16 @@
 // loaded W at a time (W = 4, 2 or 1 consecutive floats, coalesced across the
 // warp).  Each logit is turned into an order-preserving 32-bit key (-0 is
 // first mapped to +0, so keys compare exactly like the float values).
-//   * round r of top-k: every lane proposes its largest untaken key (slots
-//     are scanned in increasing expert index, so among equal keys the lowest
-//     index is proposed); the warp takes the maximum key with one
-//     redux.sync, then the minimum expert index among the lanes proposing
-//     that key with a second redux.sync; the owner marks it taken and lane r
-//     keeps it.  Equal logits therefore come out in index order;
+//   * threshold: T = the k-th largest of the 32 lane maxima (found with k
+//     rounds of redux.sync max + ballot).  The k lanes supplying those maxima
+//     hold k distinct elements >= T, so the top k all lie at or above T;
+//   * the candidates >= T (typically a dozen) are compacted through shared
+//     memory to one per lane; round r of top-k then takes the maximum key
+//     with one redux.sync and the minimum expert index among the lanes
+//     holding it with a second, and lane r keeps the winner.  Equal logits
+//     therefore come out in index order.  With fewer than 4 slots per lane,
+//     or if more than 32 candidates survive (many ties), the rounds scan every
+//     lane's slots instead (same result);
 //   * the row max m is round 0's key; with renormalisation the weights are
 //     exp(x_i - m) / sum over the k selected, otherwise exp(x_i - m) / l with
 //     l = sum over all E of exp(x - m);
@@ -49,7 +53,10 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int r
   static_assert(NV % W == 0 && NV <= 32, "layout");
   const int lane = threadIdx.x & 31;
   const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int warp = threadIdx.x >> 5;
   const int tok0 = warp_id * TPW;
+  __shared__ uint32_t sm_key[8][32];
+  __shared__ int sm_idx[8][32];
 
   uint32_t key[TPW][NV];
 #pragma unroll
@@ -87,38 +94,98 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int r
   // expert index of slot i of this lane
   auto expert = [&](int i) -> int { return (i / W) * 32 * W + lane * W + (i % W); };
 
-  uint32_t taken[TPW];
   uint32_t mykey[TPW];
   int myidx[TPW];
 #pragma unroll
   for (int t = 0; t < TPW; ++t) {
-    taken[t] = 0u;
     mykey[t] = 0u;
     myidx[t] = 0;
   }
 
-  for (int r = 0; r < k; ++r) {
 #pragma unroll
-    for (int t = 0; t < TPW; ++t) {
-      uint32_t bk = 0u;
-      int bs = -1;
+  for (int t = 0; t < TPW; ++t) {
+    // Threshold thr: the k-th largest of the 32 lane maxima.  The k lanes that
+    // supply those maxima hold k distinct elements >= thr, so every element of
+    // the top k is >= thr; everything below it is discarded.
+    uint32_t lm = 0u;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) lm = max(lm, key[t][i]);
+    uint32_t thr = 0u;
+    if (NV >= 4) {
+      uint32_t act = lm;
+      for (int r = 0; r < k; ++r) {
+        const uint32_t g = __reduce_max_sync(FULL, act);
+        const uint32_t holders = __ballot_sync(FULL, act == g);
+        if (lane == __ffs(holders) - 1) act = 0u;
+        thr = g;
+      }
+    }
+    uint32_t cmask = 0u;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) cmask |= (key[t][i] >= thr && key[t][i] != 0u ? 1u : 0u) << i;
+    const int n = __popc(cmask);
+    // exclusive prefix of the candidate counts across the warp
+    int incl = n, total = 33;
+    if (NV >= 4) {
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+      }
+      total = __shfl_sync(FULL, incl, 31);
+    }
+    uint32_t ck = 0u;      // this lane's candidate after compaction (0: none)
+    int ci = 0x7fffffff;
+    if (NV >= 4 && total <= 32) {
+      // compact the candidates to one per lane through shared memory
+      int pos = incl - n;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
-        if (!((taken[t] >> i) & 1u) && key[t][i] > bk) {
-          bk = key[t][i];
-          bs = i;
+        if ((cmask >> i) & 1u) {
+          sm_key[warp][pos] = key[t][i];
+          sm_idx[warp][pos] = expert(i);
+          ++pos;
         }
       }
-      int bi = 0x7fffffff;
+      __syncwarp();
+      if (lane < total) {
+        ck = sm_key[warp][lane];
+        ci = sm_idx[warp][lane];
+      }
+      __syncwarp();
+      for (int r = 0; r < k; ++r) {
+        const uint32_t g = __reduce_max_sync(FULL, ck);
+        const int gi = (int)__reduce_min_sync(FULL, ck == g ? (uint32_t)ci : 0x7fffffffu);
+        if (ck == g && ci == gi) ck = 0u;
+        if (lane == r) {
+          mykey[t] = g;
+          myidx[t] = gi;
+        }
+      }
+    } else {
+      // few slots per lane, or many equal values: rounds scan every slot
+      uint32_t taken = 0u;
+      for (int r = 0; r < k; ++r) {
+        uint32_t bk = 0u;
+        int bs = -1;
 #pragma unroll
-      for (int i = 0; i < NV; ++i)
-        if (i == bs) bi = expert(i);
-      const uint32_t gk = __reduce_max_sync(FULL, bk);
-      const int gi = (int)__reduce_min_sync(FULL, bk == gk ? (uint32_t)bi : 0x7fffffffu);
-      if (bs >= 0 && bk == gk && bi == gi) taken[t] |= 1u << bs;
-      if (lane == r) {
-        mykey[t] = gk;
-        myidx[t] = gi;
+        for (int i = 0; i < NV; ++i) {
+          if (!((taken >> i) & 1u) && key[t][i] > bk) {
+            bk = key[t][i];
+            bs = i;
+          }
+        }
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (i == bs) bi = expert(i);
+        const uint32_t gk = __reduce_max_sync(FULL, bk);
+        const int gi = (int)__reduce_min_sync(FULL, bk == gk ? (uint32_t)bi : 0x7fffffffu);
+        if (bs >= 0 && bk == gk && bi == gi) taken |= 1u << bs;
+        if (lane == r) {
+          mykey[t] = gk;
+          myidx[t] = gi;
+        }
       }
     }
   }

@@ -201,6 +201,26 @@ def cpu_baseline(budget_s=10.0):
                       f"float64 oracle, {elapsed:.1f} s on {pool.cores} single-threaded workers"}
 
 
+# -------------------------------------------------------- multi-rank logic --
+
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value (all ranks get it); the value itself
+    on a single rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_gbs(bytes_per_rank_step, world, ms_step):
+    """Whole-job throughput in GB/s: every rank processed its own bytes in the
+    slowest rank's time."""
+    return world * bytes_per_rank_step / (ms_step * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- GPU timing --
 
 def _events(torch, n):
@@ -409,15 +429,11 @@ def run_rf(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, "cuda")
     kern_ms = statistics.mean(ka[i].elapsed_time(kb[i]) for i in range(args.steps))
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = t.item()
     ms_step = ms_total / args.steps
     kv_bytes = 2 * R * L * D * 2
-    value = world * kv_bytes / (ms_step * 1e-3) / 1e9
+    value = job_gbs(kv_bytes, world, ms_step)
     alg_bytes = kv_bytes + R * D * 2 + R * S * (D + 2) * 4
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
 
@@ -450,13 +466,9 @@ def run_rf(args):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = t.item()
+        e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, world, "cuda")
         h2d = q.numel() * 2 + K.numel() * 2 + V.numel() * 2
-        e2e = {"value": round(world * kv_bytes / (e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        e2e = {"value": round(job_gbs(kv_bytes, world, e_ms), 1), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": out.numel() * 2,
                "ms_per_step": round(e_ms, 3), "steps": n_e2e}
         del hq, hK, hV

@@ -23,10 +23,11 @@
 //   warps 0-7   softmax of tile A, warps 8-15 softmax of tile B: two threads
 //               per query row (TMEM lane), one per 64-key half.  A thread
 //               loads its 64 scores, the halves exchange partial row maxima
-//               through shared memory (an mbarrier per tile and step, bounded
-//               like every other wait), then each thread exponentiates its
-//               keys in the log2 domain (scores times scale*log2(e)), writes
-//               its half of P, and rescales its half of O when needed.
+//               through shared memory (an mbarrier per tile, row quarter and
+//               step, bounded like every other wait), then each thread
+//               exponentiates its keys in the log2 domain (scores times
+//               scale*log2(e)), writes its half of P, and rescales its half
+//               of O when needed.
 // Rescaling is lazy: the reference max m_ref of a row moves (and O and l are
 // multiplied by exp2(m_ref_old - m_ref_new)) only when the tile max exceeds
 // it by more than 8, so p <= 2^8.  The result is the same mathematics (O and
@@ -62,7 +63,7 @@ struct Shared {
   uint64_t s_full[2];          // per tile
   uint64_t p_ready[2];         // per tile, 8 softmax warps
   uint64_t o_done[2];          // per tile
-  uint64_t max_ready[2];       // per tile, 8 softmax warps, one phase per step
+  uint64_t max_ready[2][4];    // per tile and row quarter (2 warps), one phase per step
   uint64_t l_ready[2];         // per tile, 8 softmax warps
   float pmax[2][2][2][BM];     // [tile][step parity][half][row]
   float l_part[2][2][BM];      // [tile][half][row]
@@ -147,7 +148,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tc::mbar_init(&sh->s_full[x], 1);
       tc::mbar_init(&sh->p_ready[x], 8);
       tc::mbar_init(&sh->o_done[x], 1);
-      tc::mbar_init(&sh->max_ready[x], 8);
+      for (int q4 = 0; q4 < 4; ++q4)
+        tc::mbar_init(&sh->max_ready[x][q4], 2);
       tc::mbar_init(&sh->l_ready[x], 8);
     }
     sh->abort = 0;
@@ -269,8 +271,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       // exchange with the other half of the row
       sh->pmax[x][j & 1][half][r] = pm;
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->max_ready[x]);
-      if (!tc::mbar_wait(&sh->max_ready[x], (uint32_t)j & 1u, abort)) {
+      // the two warps that share this row quarter
+      if (lane == 0) tc::mbar_arrive(&sh->max_ready[x][quarter]);
+      if (!tc::mbar_wait(&sh->max_ready[x][quarter], (uint32_t)j & 1u, abort)) {
         ok = false;
         break;
       }

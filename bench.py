@@ -187,6 +187,72 @@ class OracleDecodePool:
         self.pool.join()
 
 
+def _oracle_path_samples(budget_s):
+    """Runs in a spawned single-threaded worker: the float64 oracle of each
+    cascade on a bounded sample of its workload, timed.  Returns
+    {path: (units_done, unit, seconds, sample description)}."""
+    import torch
+    import synthetic_inputs as si
+    from oracle import attention, bf16, fp8, routing
+
+    def timed(fn):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= budget_s:
+                return n, dt
+
+    res = {}
+    q, K, V = (t.double().numpy() for t in si.decode_inputs(1, 4096, 64, torch.float32, seed=1))
+    n, dt = timed(lambda: attention.softmax_v_rows(q, K, V, 0.125))
+    res["single_row_decode_f32"] = (n * 2 * 4096 * 64 * 4, "B", dt, "the whole q[64], K, V [4096, 64]")
+    for name, tokens in (("route_256", 2048), ("route_64", 8192)):
+        cfg = si.FULL[name]
+        x = si.routing_logits(tokens, cfg["E"], seed=si.SEEDS[name]).numpy()
+        n, dt = timed(lambda: routing.softmax_topk(x, cfg["k"], True))
+        res["routing_%dx%d_top%d" % (cfg["T"], cfg["E"], cfg["k"])] = (
+            n * tokens * (cfg["E"] * 4 + cfg["k"] * 8), "B", dt,
+            f"{tokens} of the {cfg['T']} tokens")
+    cfg = si.FULL["quant_gemm"]
+    xb, wq, sw = si.quant_gemm_inputs(cfg["M"], cfg["K"], cfg["N"], seed=4)
+    xs = bf16.decode(xb[:256].view(torch.int16).numpy())
+    n, dt = timed(lambda: fp8.absmax_quant(xs))
+    res["absmax_quant_e4m3"] = (n * 256 * cfg["K"] * 3, "B", dt, f"256 of the {cfg['M']} rows")
+    xq, sx = fp8.absmax_quant(bf16.decode(xb[:32].view(torch.int16).numpy()))
+    wqn, swn = wq.numpy(), sw.numpy()
+    n, dt = timed(lambda: fp8.scaled_gemm(xq, sx, wqn, swn))
+    res["fp8_gemm"] = (n * 2.0 * 32 * cfg["N"] * cfg["K"], "FLOP", dt,
+                       f"32 of the {cfg['M']} rows against all of Wq")
+    cfg = si.FULL["prefill"]
+    Q, Kp, Vp = si.prefill_inputs(1, 1, cfg["N"], cfg["D"], seed=5)
+    Q, Kp, Vp = (t[0, 0].double().numpy() for t in (Q, Kp, Vp))
+    rows = list(range(cfg["N"] // 2, cfg["N"] // 2 + 16))
+    n, dt = timed(lambda: [attention.causal_attention_row(Q[i], Kp, Vp, cfg["D"] ** -0.5, i)
+                           for i in rows])
+    res["causal_prefill"] = (n * sum(4.0 * cfg["D"] * (i + 1) for i in rows), "FLOP", dt,
+                             "16 query rows in the middle of one head (exact causal FLOPs)")
+    return res
+
+
+def oracle_path_baselines(budget_s=1.5):
+    """The oracle beside each GPU path, in one single-threaded spawned worker."""
+    import multiprocessing as mp
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    with mp.get_context("spawn").Pool(1) as pool:
+        res = pool.apply(_oracle_path_samples, (budget_s,))
+    out = {}
+    for path, (units, unit, dt, sample) in res.items():
+        if unit == "B":
+            out[path] = {"value": round(units / dt / 1e9, 4), "unit": "GB/s"}
+        else:
+            out[path] = {"value": round(units / dt / 1e12, 6), "unit": "TFLOP/s"}
+        out[path].update({"cores": 1, "kind": "oracle", "sample": sample + f", {dt:.1f} s"})
+    return out
+
+
 def cpu_baseline(budget_s=10.0):
     pool = OracleDecodePool()
     rows, elapsed = 0, 0.0
@@ -274,9 +340,11 @@ def path_single_row(torch, rf, peaks):
         rf.rf_state_merge(sm, sl, sa, out)
     ms = time_graph(torch, [call] * 50, 20)
     nbytes = 2 * cfg["L"] * cfg["D"] * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": "single-row decode fp32 q[64] K,V[4096,64], S=32 (latency bound; "
                         "graph of 50 back-to-back calls, inputs L2-resident)",
-            "value": round(nbytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2)}
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+            "roofline": roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", None)}
 
 
 def path_routing(torch, rf, peaks, name):
@@ -490,6 +558,10 @@ def run_rf(args):
             torch.cuda.empty_cache()
 
     cpu = cpu_baseline(args.cpu_budget) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if paths and rank == 0 and not args.no_cpu:
+        for name, base in oracle_path_baselines().items():
+            if name in paths and isinstance(paths[name], dict) and "value" in paths[name]:
+                paths[name]["cpu_oracle"] = base
 
     if rank == 0:
         line = {

@@ -20,6 +20,8 @@ float64 (numpy), exactly as the pages state the stages:
   fused).
 * FP8 per-token quantisation then GEMM -- abs-max, scale = absmax / 448, e4m3
   encode, then the GEMM sum (transcript cue 33).
+* single-row cascades -- safe softmax of a row, variance, moment of inertia
+  (transcript cue 47).
 
 Every floating-point step is float64 unless the step itself is a rounding to a
 narrower format the method fixes (fp32 scale and fp32 quotient before the e4m3
@@ -32,4 +34,4 @@ scaled-dot-product attention, torch's own float8/bfloat16 casts), the e4m3
 definition checked exhaustively, and brute force on tiny inputs.
 """
 
-from . import attention, routing, fp8, bf16  # noqa: F401
+from . import attention, routing, fp8, bf16, rowcascades  # noqa: F401

@@ -1,0 +1,76 @@
+"""Pins for the single-row cascade oracles (CPU only): library routines
+(torch float64 softmax, numpy var), closed forms (uniform rows, arithmetic
+sequences, two masses, rings), invariants (shift invariance, the parallel-
+axis theorem) and brute force on tiny inputs."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import rowcascades as rc
+
+
+def test_softmax_matches_torch_and_invariants():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((7, 1000)) * 3
+    y = rc.row_softmax(x)
+    np.testing.assert_allclose(y, torch.softmax(torch.from_numpy(x), dim=1).numpy(), rtol=1e-13)
+    np.testing.assert_allclose(y.sum(axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(rc.row_softmax(x + 123.0), y, rtol=1e-12)   # shift invariance
+    u = rc.row_softmax(np.full((2, 64), -4.0))
+    np.testing.assert_allclose(u, 1 / 64, rtol=1e-15)
+
+
+def test_variance_closed_forms_and_numpy():
+    n = 4097
+    x = np.arange(n, dtype=np.float64)[None, :]
+    mean, var = rc.row_variance(x)
+    assert mean[0] == (n - 1) / 2
+    assert var[0] == pytest.approx((n * n - 1) / 12, rel=1e-14)
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal((5, 333)) * 7 + 2
+    mean, var = rc.row_variance(y)
+    np.testing.assert_allclose(mean, y.mean(axis=1), rtol=1e-13)
+    np.testing.assert_allclose(var, y.var(axis=1), rtol=1e-12)
+    _, v0 = rc.row_variance(np.full((1, 50), 3.25))
+    assert v0[0] == 0.0
+    _, vs = rc.row_variance(y + 1e3)
+    np.testing.assert_allclose(vs, var, rtol=1e-9)
+
+
+def test_moment_of_inertia_closed_forms():
+    # two unit masses a distance d apart: each sits d/2 from the centre
+    d = 3.0
+    mass = np.array([[1.0, 1.0]])
+    pos = np.zeros((1, 3, 2))
+    pos[0, 0] = [0.0, d]
+    c, inertia = rc.moment_of_inertia(mass, pos)
+    np.testing.assert_allclose(c[0], [d / 2, 0, 0])
+    assert inertia[0] == pytest.approx(d * d / 2)
+    # ring of equal masses of radius rho around (1, 2, 3): I = M rho^2
+    k, rho = 360, 2.5
+    t = np.arange(k) * 2 * math.pi / k
+    pos = np.stack([1 + rho * np.cos(t), 2 + rho * np.sin(t), np.full(k, 3.0)])[None]
+    mass = np.full((1, k), 0.5)
+    c, inertia = rc.moment_of_inertia(mass, pos)
+    np.testing.assert_allclose(c[0], [1, 2, 3], atol=1e-12)
+    assert inertia[0] == pytest.approx(0.5 * k * rho * rho, rel=1e-12)
+
+
+def test_moment_of_inertia_parallel_axis_and_brute_force():
+    rng = np.random.default_rng(2)
+    R, n = 4, 9
+    mass = rng.uniform(0.1, 2.0, (R, n))
+    pos = rng.standard_normal((R, 3, n))
+    c, inertia = rc.moment_of_inertia(mass, pos)
+    for r in range(R):
+        M = sum(mass[r])
+        cx = [sum(mass[r][i] * pos[r][a][i] for i in range(n)) / M for a in range(3)]
+        ii = sum(mass[r][i] * sum((pos[r][a][i] - cx[a]) ** 2 for a in range(3)) for i in range(n))
+        np.testing.assert_allclose(c[r], cx, rtol=1e-12)
+        assert inertia[r] == pytest.approx(ii, rel=1e-12)
+        # parallel-axis theorem: about the origin = about the centre + M |c|^2
+        about_origin = sum(mass[r][i] * sum(pos[r][a][i] ** 2 for a in range(3)) for i in range(n))
+        assert about_origin == pytest.approx(inertia[r] + M * sum(v * v for v in cx), rel=1e-12)

@@ -430,6 +430,48 @@ def path_prefill(torch, rf, peaks):
             "roofline": roofline("tensor", tf, peaks["bf16_tflops"], "TFLOP/s", ncu_traffic("prefill"))}
 
 
+def path_row_cascades(torch, rf, peaks):
+    """Single-row cascades at every fusion level: softmax rows of 1K-8K
+    (256 MB in, 256 MB out), variance of [16384 x 4096], moment of inertia of
+    [4096 x 4096] points (256 MB); all larger than L2."""
+    names = {0: "unfused", 1: "thread", 2: "warp", 3: "block"}
+    g = torch.Generator(device="cuda").manual_seed(11)
+    res = {"softmax": {}, "variance": {}, "inertia": {}}
+
+    def entry(ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+
+    for n in (1024, 2048, 4096, 8192):
+        R = (1 << 26) // n
+        x = torch.randn(R, n, device="cuda", generator=g)
+        y = torch.empty_like(x)
+        work = torch.empty(2 * R, device="cuda")
+        res["softmax"][f"n{n}"] = {}
+        for lvl, nm in names.items():
+            ms = time_graph(torch, [lambda: rf.rf_row_softmax(x, y, lvl, work)] * 5, 5)
+            res["softmax"][f"n{n}"][nm] = entry(ms, 2 * R * n * 4)
+        del x, y, work
+    xv = torch.randn(16384, 4096, device="cuda", generator=g)
+    mean = torch.empty(16384, device="cuda")
+    var = torch.empty(16384, device="cuda")
+    for lvl, nm in names.items():
+        ms = time_graph(torch, [lambda: rf.rf_row_variance(xv, mean, var, lvl)] * 5, 5)
+        res["variance"][nm] = entry(ms, xv.numel() * 4)
+    del xv
+    mass = torch.rand(4096, 4096, device="cuda", generator=g) + 0.05
+    pos = torch.randn(4096, 3, 4096, device="cuda", generator=g)
+    cen = torch.empty(4096, 3, device="cuda")
+    ine = torch.empty(4096, device="cuda")
+    for lvl, nm in names.items():
+        ms = time_graph(torch, [lambda: rf.rf_moment_of_inertia(mass, pos, cen, ine, lvl)] * 5, 5)
+        res["inertia"][nm] = entry(ms, (mass.numel() + pos.numel()) * 4)
+    res["workload"] = ("row softmax R = 2^26/n rows of n fp32 (read + write counted); variance "
+                       "x [16384, 4096]; moment of inertia mass [4096, 4096] + pos [4096, 3, 4096]; "
+                       "CUDA graphs of 5 calls, inputs larger than L2")
+    return res
+
+
 # --------------------------------------------------------------------- arms --
 
 def run_rf(args):
@@ -458,7 +500,8 @@ def run_rf(args):
                "routing_64": lambda: path_routing(torch, rf, peaks, "route_64"),
                "quant": lambda: path_quant(torch, rf, peaks),
                "gemm": lambda: path_gemm(torch, rf, peaks),
-               "prefill": lambda: path_prefill(torch, rf, peaks)}
+               "prefill": lambda: path_prefill(torch, rf, peaks),
+               "rows": lambda: path_row_cascades(torch, rf, peaks)}
         print(json.dumps({args.only: fns[args.only]()}), flush=True)
         return
     B, H, L, D = DECODE["B"], DECODE["H"], DECODE["L"], DECODE["D"]
@@ -550,7 +593,8 @@ def run_rf(args):
                          ("routing_65536x64_top2", lambda: path_routing(torch, rf, peaks, "route_64")),
                          ("absmax_quant_e4m3", lambda: path_quant(torch, rf, peaks)),
                          ("fp8_gemm", lambda: path_gemm(torch, rf, peaks)),
-                         ("causal_prefill", lambda: path_prefill(torch, rf, peaks))):
+                         ("causal_prefill", lambda: path_prefill(torch, rf, peaks)),
+                         ("row_cascades", lambda: path_row_cascades(torch, rf, peaks))):
             try:
                 paths[name] = fn()
             except Exception as e:         # report, never hide: the line says what failed
@@ -634,7 +678,7 @@ def main():
                     help="decode rows instead of B*H=1024 (small cases for ncu captures)")
     ap.add_argument("--decode-only", action="store_true", help="skip the other cascades")
     ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm",
-                                       "prefill"], help="time one other cascade alone")
+                                       "prefill", "rows"], help="time one other cascade alone")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work")

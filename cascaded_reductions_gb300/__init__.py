@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "librf.so")
 
 RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_MISALIGNED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(6)
 RF_F32, RF_BF16 = 0, 1
+RF_FUSE_NONE, RF_FUSE_THREAD, RF_FUSE_WARP, RF_FUSE_BLOCK = range(4)
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -41,6 +42,9 @@ _SIGNATURES = {
     "rf_fp8_gemm_scaled": (_I, [_P, _P, _P, _P, _I, _I, _I, _P, _P]),
     "rf_device_error": (_I, [ctypes.POINTER(_I), _P]),
     "rf_attn_decode_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P, _P]),
+    "rf_row_softmax": (_I, [_P, _I, _I, _P, _I, _P, _P]),
+    "rf_row_variance": (_I, [_P, _I, _I, _P, _P, _I, _P]),
+    "rf_moment_of_inertia": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
 }
 
 
@@ -211,6 +215,38 @@ def rf_attn_decode_noalloc(q, k, v, S, scale, out, lse=None, stream=None):
     _check(_lib.rf_attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale),
                                        _dtype_code(k.dtype), _ptr(out), _dtype_code(out.dtype),
                                        _ptr(lse), _stream(stream)), "rf_attn_decode_noalloc")
+
+
+def rf_row_softmax(x, y, level, work=None, stream=None):
+    """x, y [R, n] fp32; work [2R] fp32 for RF_FUSE_NONE."""
+    R, n = x.shape
+    _need(x, torch.float32, "x")
+    _need(y, torch.float32, "y", (R, n))
+    if work is not None:
+        _need(work, torch.float32, "work", (2 * R,))
+    _check(_lib.rf_row_softmax(_ptr(x), R, n, _ptr(y), int(level), _ptr(work), _stream(stream)),
+           "rf_row_softmax")
+
+
+def rf_row_variance(x, mean, var, level, stream=None):
+    """x [R, n] fp32 -> mean [R], var [R] (population variance)."""
+    R, n = x.shape
+    _need(x, torch.float32, "x")
+    _need(mean, torch.float32, "mean", (R,))
+    _need(var, torch.float32, "var", (R,))
+    _check(_lib.rf_row_variance(_ptr(x), R, n, _ptr(mean), _ptr(var), int(level),
+                                _stream(stream)), "rf_row_variance")
+
+
+def rf_moment_of_inertia(mass, pos, center, inertia, level, stream=None):
+    """mass [R, n], pos [R, 3, n] fp32 -> center [R, 3], inertia [R]."""
+    R, n = mass.shape
+    _need(mass, torch.float32, "mass")
+    _need(pos, torch.float32, "pos", (R, 3, n))
+    _need(center, torch.float32, "center", (R, 3))
+    _need(inertia, torch.float32, "inertia", (R,))
+    _check(_lib.rf_moment_of_inertia(_ptr(mass), _ptr(pos), R, n, _ptr(center), _ptr(inertia),
+                                     int(level), _stream(stream)), "rf_moment_of_inertia")
 
 
 def rf_device_error(stream=None):

@@ -108,6 +108,42 @@ rf_status rf_absmax_quant_fp8_gemm(const void* x, int M, int K, const uint8_t* w
   return rf::launch_fp8_gemm(xq, sx, wq, sw, M, N, K, y, as_stream(stream));
 }
 
+static rf_status check_row_args(int R, int n, int level) {
+  if (R <= 0 || n <= 0) return RF_ERR_INVALID_ARG;
+  if (level < RF_FUSE_NONE || level > RF_FUSE_BLOCK) return RF_ERR_INVALID_ARG;
+  if (n % 4 != 0) return RF_ERR_UNSUPPORTED;
+  return RF_OK;
+}
+
+rf_status rf_row_softmax(const float* x, int R, int n, float* y, int level, float* work,
+                         void* stream) {
+  if (!x || !y) return RF_ERR_INVALID_ARG;
+  rf_status s = check_row_args(R, n, level);
+  if (s != RF_OK) return s;
+  if (level == RF_FUSE_NONE && !work) return RF_ERR_INVALID_ARG;
+  if (level != RF_FUSE_NONE && n > 8192) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(x) || !rf::aligned16(y)) return RF_ERR_MISALIGNED;
+  return rf::launch_row_softmax(x, R, n, y, level, work, as_stream(stream));
+}
+
+rf_status rf_row_variance(const float* x, int R, int n, float* mean, float* var, int level,
+                          void* stream) {
+  if (!x || !mean || !var) return RF_ERR_INVALID_ARG;
+  rf_status s = check_row_args(R, n, level);
+  if (s != RF_OK) return s;
+  if (!rf::aligned16(x)) return RF_ERR_MISALIGNED;
+  return rf::launch_row_variance(x, R, n, mean, var, level, as_stream(stream));
+}
+
+rf_status rf_moment_of_inertia(const float* mass, const float* pos, int R, int n, float* center,
+                               float* inertia, int level, void* stream) {
+  if (!mass || !pos || !center || !inertia) return RF_ERR_INVALID_ARG;
+  rf_status s = check_row_args(R, n, level);
+  if (s != RF_OK) return s;
+  if (!rf::aligned16(mass) || !rf::aligned16(pos)) return RF_ERR_MISALIGNED;
+  return rf::launch_moment_of_inertia(mass, pos, R, n, center, inertia, level, as_stream(stream));
+}
+
 rf_status rf_device_error(int* status, void* stream) {
   if (!status) return RF_ERR_INVALID_ARG;
   return rf::read_device_error(status, as_stream(stream));

@@ -70,6 +70,12 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
                           int M, int N, int K, void* y, cudaStream_t st);
 rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
                          int causal, float scale, void* out, float* lse, cudaStream_t st);
+rf_status launch_row_softmax(const float* x, int R, int n, float* y, int level, float* work,
+                             cudaStream_t st);
+rf_status launch_row_variance(const float* x, int R, int n, float* mean, float* var, int level,
+                              cudaStream_t st);
+rf_status launch_moment_of_inertia(const float* mass, const float* pos, int R, int n,
+                                   float* center, float* inertia, int level, cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);
 // read and clear the bounded-wait status word of each tensor-core kernel file
 rf_status gemm_take_status(int* status);

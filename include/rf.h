@@ -202,6 +202,42 @@ rf_status rf_fp8_gemm_scaled(const uint8_t* xq, const float* sx, const uint8_t* 
                              const float* sw, int M, int N, int K, void* y, void* stream);
 
 /*
+ * Single-row cascades (transcript cue 47: safe softmax of 1K-8K-element rows
+ * at several fusion levels; variance; moment of inertia).  One row per CTA.
+ * `level` selects where in the reduction tree the incremental state is kept:
+ *   RF_FUSE_NONE    unfused: one kernel per reduction, each re-reading the row
+ *   RF_FUSE_THREAD  each thread folds its elements one by one into a state,
+ *                   thread states are merged at the end
+ *   RF_FUSE_WARP    each warp folds 128-element tiles into a warp state
+ *   RF_FUSE_BLOCK   the block folds 1024-element tiles into one block state
+ * All levels compute the same result (up to fp32 rounding order).
+ * Rows hold n fp32 values, n % 4 == 0 (RF_ERR_UNSUPPORTED otherwise).
+ */
+typedef enum { RF_FUSE_NONE = 0, RF_FUSE_THREAD = 1, RF_FUSE_WARP = 2, RF_FUSE_BLOCK = 3 } rf_fusion_level;
+
+/* rf_row_softmax -- y = softmax(x) per row: max, then sum of exp(x - max),
+ * then the divide (transcript cue 9).
+ *   x, y  [R, n] fp32 (y may not alias x)
+ *   work  [2R] fp32 scratch for RF_FUSE_NONE (row max and sum), else may be NULL
+ * Fused levels hold the row in registers: n <= 8192 (RF_ERR_UNSUPPORTED above). */
+rf_status rf_row_softmax(const float* x, int R, int n, float* y, int level, float* work,
+                         void* stream);
+
+/* rf_row_variance -- population variance per row: mean = sum x / n, then
+ * var = sum (x - mean)^2 / n; fused levels merge (count, mean, M2) states.
+ *   x [R, n] fp32;  mean [R], var [R] fp32 out */
+rf_status rf_row_variance(const float* x, int R, int n, float* mean, float* var, int level,
+                          void* stream);
+
+/* rf_moment_of_inertia -- per row of n point masses: centre of mass
+ * c = sum m p / sum m, then I = sum m |p - c|^2 (about the centre of mass);
+ * fused levels merge (M, c, I) states by the parallel-axis theorem.
+ *   mass [R, n] fp32 (positive);  pos [R, 3, n] fp32 (x, y, z coordinates of
+ *   each row stored one after the other);  center [R, 3], inertia [R] fp32 out */
+rf_status rf_moment_of_inertia(const float* mass, const float* pos, int R, int n, float* center,
+                               float* inertia, int level, void* stream);
+
+/*
  * rf_device_error -- status of the bounded on-device waits.  The
  * tensor-core kernels wait on shared-memory barriers with an iteration
  * limit; a wait that runs out records RF_ERR_TIMEOUT in a device word and

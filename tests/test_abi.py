@@ -137,3 +137,22 @@ def test_binding_declares_every_symbol():
     """The Python binding wraps every entry point the header declares."""
     import cascaded_reductions_gb300 as rf
     assert set(rf._SIGNATURES) == set(declared_symbols())
+
+
+def test_row_cascade_validation(lib):
+    sm = lib.rf_row_softmax
+    assert sm(NULL, 4, 1024, FAKE, 1, NULL, NULL) == 1
+    assert sm(FAKE, 0, 1024, FAKE, 1, NULL, NULL) == 1
+    assert sm(FAKE, 4, 1024, FAKE, 7, NULL, NULL) == 1       # unknown level
+    assert sm(FAKE, 4, 1024, FAKE, 0, NULL, NULL) == 1       # unfused needs work
+    assert sm(FAKE, 4, 1022, FAKE, 1, NULL, NULL) == 2       # n % 4
+    assert sm(FAKE, 4, 8196, FAKE, 3, NULL, NULL) == 2       # fused rows live in registers
+    assert sm(ODD, 4, 1024, FAKE, 2, NULL, NULL) == 3
+    var = lib.rf_row_variance
+    assert var(FAKE, 4, 64, NULL, FAKE, 1, NULL) == 1
+    assert var(FAKE, 4, 66, FAKE, FAKE, 1, NULL) == 2
+    assert var(FAKE, 4, 64, FAKE, FAKE, -1, NULL) == 1
+    moi = lib.rf_moment_of_inertia
+    assert moi(FAKE, FAKE, 4, 64, FAKE, NULL, 1, NULL) == 1
+    assert moi(FAKE, FAKE, 4, 6, FAKE, FAKE, 1, NULL) == 2
+    assert moi(FAKE, ODD, 4, 64, FAKE, FAKE, 1, NULL) == 3

@@ -436,7 +436,7 @@ def path_row_cascades(torch, rf, peaks):
     [4096 x 4096] points (256 MB); all larger than L2."""
     names = {0: "unfused", 1: "thread", 2: "warp", 3: "block"}
     g = torch.Generator(device="cuda").manual_seed(11)
-    res = {"softmax": {}, "variance": {}, "inertia": {}}
+    res = {"softmax": {}, "variance": {}, "inertia": {}, "layer_norm": {}}
 
     def entry(ms, nbytes):
         gbs = nbytes / (ms * 1e-3) / 1e9
@@ -466,8 +466,20 @@ def path_row_cascades(torch, rf, peaks):
     for lvl, nm in names.items():
         ms = time_graph(torch, [lambda: rf.rf_moment_of_inertia(mass, pos, cen, ine, lvl)] * 5, 5)
         res["inertia"][nm] = entry(ms, (mass.numel() + pos.numel()) * 4)
+    del mass, pos
+    xl = torch.randn(16384, 4096, device="cuda", generator=g)
+    yl = torch.empty_like(xl)
+    gam = torch.randn(4096, device="cuda", generator=g)
+    bet = torch.randn(4096, device="cuda", generator=g)
+    wl = torch.empty(2 * 16384, device="cuda")
+    res["layer_norm"] = {}
+    for lvl, nm in ((0, "unfused"), (1, "fused")):
+        ms = time_graph(torch, [lambda: rf.rf_layer_norm(xl, gam, bet, 1e-5, yl, lvl, wl)] * 5, 5)
+        res["layer_norm"][nm] = entry(ms, 2 * xl.numel() * 4)
+    del xl, yl
     res["workload"] = ("row softmax R = 2^26/n rows of n fp32 (read + write counted); variance "
                        "x [16384, 4096]; moment of inertia mass [4096, 4096] + pos [4096, 3, 4096]; "
+                       "layer norm x, y [16384, 4096] (read + write counted); "
                        "CUDA graphs of 5 calls, inputs larger than L2")
     return res
 

@@ -45,6 +45,7 @@ _SIGNATURES = {
     "rf_row_softmax": (_I, [_P, _I, _I, _P, _I, _P, _P]),
     "rf_row_variance": (_I, [_P, _I, _I, _P, _P, _I, _P]),
     "rf_moment_of_inertia": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
+    "rf_layer_norm": (_I, [_P, _P, _P, _I, _I, _F, _P, _I, _P, _P]),
 }
 
 
@@ -247,6 +248,19 @@ def rf_moment_of_inertia(mass, pos, center, inertia, level, stream=None):
     _need(inertia, torch.float32, "inertia", (R,))
     _check(_lib.rf_moment_of_inertia(_ptr(mass), _ptr(pos), R, n, _ptr(center), _ptr(inertia),
                                      int(level), _stream(stream)), "rf_moment_of_inertia")
+
+
+def rf_layer_norm(x, gamma, beta, eps, y, level, work=None, stream=None):
+    """x, y [R, n] fp32; gamma, beta [n]; work [2R] fp32 for RF_FUSE_NONE."""
+    R, n = x.shape
+    _need(x, torch.float32, "x")
+    _need(gamma, torch.float32, "gamma", (n,))
+    _need(beta, torch.float32, "beta", (n,))
+    _need(y, torch.float32, "y", (R, n))
+    if work is not None:
+        _need(work, torch.float32, "work", (2 * R,))
+    _check(_lib.rf_layer_norm(_ptr(x), _ptr(gamma), _ptr(beta), R, n, float(eps), _ptr(y),
+                              int(level), _ptr(work), _stream(stream)), "rf_layer_norm")
 
 
 def rf_device_error(stream=None):

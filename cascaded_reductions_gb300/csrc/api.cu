@@ -144,6 +144,19 @@ rf_status rf_moment_of_inertia(const float* mass, const float* pos, int R, int n
   return rf::launch_moment_of_inertia(mass, pos, R, n, center, inertia, level, as_stream(stream));
 }
 
+rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
+                        float eps, float* y, int level, float* work, void* stream) {
+  if (!x || !gamma || !beta || !y) return RF_ERR_INVALID_ARG;
+  rf_status s = check_row_args(R, n, level);
+  if (s != RF_OK) return s;
+  if (!(eps >= 0.f) || !isfinite(eps)) return RF_ERR_INVALID_ARG;
+  if (level == RF_FUSE_NONE && !work) return RF_ERR_INVALID_ARG;
+  if (level != RF_FUSE_NONE && n > 8192) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(x) || !rf::aligned16(y) || !rf::aligned16(gamma) || !rf::aligned16(beta))
+    return RF_ERR_MISALIGNED;
+  return rf::launch_layer_norm(x, gamma, beta, R, n, eps, y, level, work, as_stream(stream));
+}
+
 rf_status rf_device_error(int* status, void* stream) {
   if (!status) return RF_ERR_INVALID_ARG;
   return rf::read_device_error(status, as_stream(stream));

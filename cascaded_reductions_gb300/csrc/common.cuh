@@ -76,6 +76,8 @@ rf_status launch_row_variance(const float* x, int R, int n, float* mean, float* 
                               cudaStream_t st);
 rf_status launch_moment_of_inertia(const float* mass, const float* pos, int R, int n,
                                    float* center, float* inertia, int level, cudaStream_t st);
+rf_status launch_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
+                            float eps, float* y, int level, float* work, cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);
 // read and clear the bounded-wait status word of each tensor-core kernel file
 rf_status gemm_take_status(int* status);

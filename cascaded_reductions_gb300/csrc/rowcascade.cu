@@ -1,7 +1,9 @@
 // Single-row cascades at several fusion levels: safe softmax of a row,
 // variance, moment of inertia (RedFuser episode transcript, cue 47: safe
 // softmax over 1K-8K elements at thread, warp and block fusion levels, and
-// variance and moment of inertia as further cascades).
+// variance and moment of inertia as further cascades), and layer
+// normalisation (the bookshelf explainer's "Problem" section names
+// normalisation layers among the cascaded reductions).
 //
 // Every cascade here has two dependent reductions; the fused forms carry a
 // mergeable state through one read of the row (cue 31: rescale the state for
@@ -541,6 +543,75 @@ inertia_from_center_kernel(const float* __restrict__ mass, const float* __restri
   if (threadIdx.x == 0) inertia[blockIdx.x] = I;
 }
 
+// --------------------------------------------------- layer normalisation ----
+// Fused: the row stays in registers; each thread reduces its values to
+// (count, mean, M2) in two passes over registers, the states merge across the
+// block, and the same registers are normalised and written.
+template <int VPT>
+__global__ void __launch_bounds__(TH)
+layernorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                       const float* __restrict__ beta, int n, float eps, float* __restrict__ y) {
+  __shared__ VarState red_v[NW];
+  const int n4 = n >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
+  float4* yr = reinterpret_cast<float4*>(y + (size_t)blockIdx.x * n);
+  float4 v[VPT];
+  float cnt = 0.f, sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * TH + threadIdx.x;
+    v[i] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < n4) {
+      cnt += 4.f;
+      sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+  }
+  VarState st{cnt, cnt > 0.f ? sum / cnt : 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    if (i * TH + (int)threadIdx.x < n4) {
+      const float dx = v[i].x - st.mean, dy = v[i].y - st.mean, dz = v[i].z - st.mean,
+                  dw = v[i].w - st.mean;
+      st.m2 += (dx * dx + dy * dy) + (dz * dz + dw * dw);
+    }
+  }
+  st = var_warp_merge(st);
+  if ((threadIdx.x & 31) == 0) red_v[threadIdx.x >> 5] = st;
+  __syncthreads();
+  VarState r = red_v[0];
+#pragma unroll
+  for (int w = 1; w < NW; ++w) r = var_merge(r, red_v[w]);
+  const float mu = r.mean, rstd = rsqrtf(r.m2 / (float)n + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  const float4* b4 = reinterpret_cast<const float4*>(beta);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * TH + threadIdx.x;
+    if (c < n4) {
+      const float4 g = __ldg(g4 + c), b = __ldg(b4 + c);
+      __stcs(yr + c, make_float4((v[i].x - mu) * rstd * g.x + b.x, (v[i].y - mu) * rstd * g.y + b.y,
+                                 (v[i].z - mu) * rstd * g.z + b.z, (v[i].w - mu) * rstd * g.w + b.w));
+    }
+  }
+}
+
+// unfused: mean kernel, variance kernel (both re-read the row), then normalise
+__global__ void __launch_bounds__(TH)
+layernorm_apply_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                       const float* __restrict__ beta, int n, float eps, int R,
+                       const float* __restrict__ work, float* __restrict__ y) {
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
+  float4* yr = reinterpret_cast<float4*>(y + (size_t)blockIdx.x * n);
+  const float mu = work[blockIdx.x], rstd = rsqrtf(work[R + blockIdx.x] + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  const float4* b4 = reinterpret_cast<const float4*>(beta);
+  for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    const float4 v = __ldcs(xr + c), g = __ldg(g4 + c), b = __ldg(b4 + c);
+    __stcs(yr + c, make_float4((v.x - mu) * rstd * g.x + b.x, (v.y - mu) * rstd * g.y + b.y,
+                               (v.z - mu) * rstd * g.z + b.z, (v.w - mu) * rstd * g.w + b.w));
+  }
+}
+
 template <int LEVEL>
 void launch_softmax_level(const float* x, int R, int n, float* y, cudaStream_t st) {
   const int vpt = (n / 4 + TH - 1) / TH;
@@ -563,6 +634,22 @@ rf_status launch_row_softmax(const float* x, int R, int n, float* y, int level, 
     case RF_FUSE_THREAD: launch_softmax_level<RF_FUSE_THREAD>(x, R, n, y, st); break;
     case RF_FUSE_WARP: launch_softmax_level<RF_FUSE_WARP>(x, R, n, y, st); break;
     default: launch_softmax_level<RF_FUSE_BLOCK>(x, R, n, y, st); break;
+  }
+  return launch_status();
+}
+
+rf_status launch_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
+                            float eps, float* y, int level, float* work, cudaStream_t st) {
+  if (level == RF_FUSE_NONE) {
+    mean_kernel<<<R, TH, 0, st>>>(x, n, work);
+    var_from_mean_kernel<<<R, TH, 0, st>>>(x, n, work, work + R);
+    layernorm_apply_kernel<<<R, TH, 0, st>>>(x, gamma, beta, n, eps, R, work, y);
+  } else {
+    const int vpt = (n / 4 + TH - 1) / TH;
+    if (vpt <= 1) layernorm_fused_kernel<1><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
+    else if (vpt <= 2) layernorm_fused_kernel<2><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
+    else if (vpt <= 4) layernorm_fused_kernel<4><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
+    else layernorm_fused_kernel<8><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
   }
   return launch_status();
 }

@@ -237,6 +237,17 @@ rf_status rf_row_variance(const float* x, int R, int n, float* mean, float* var,
 rf_status rf_moment_of_inertia(const float* mass, const float* pos, int R, int n, float* center,
                                float* inertia, int level, void* stream);
 
+/* rf_layer_norm -- y = (x - mean) / sqrt(var + eps) * gamma + beta per row:
+ * mean, then variance (needs the mean), then the normalisation (needs both)
+ * (the bookshelf explainer's "Problem" section lists normalisation layers
+ * among the cascaded reductions).  RF_FUSE_NONE runs one kernel per stage,
+ * each re-reading the row; any other level runs the fused single-read kernel
+ * (the row stays in registers, n <= 8192).
+ *   x, y [R, n] fp32;  gamma, beta [n] fp32;  eps >= 0
+ *   work [2R] fp32 scratch for RF_FUSE_NONE (row mean and variance), else may be NULL */
+rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
+                        float eps, float* y, int level, float* work, void* stream);
+
 /*
  * rf_device_error -- status of the bounded on-device waits.  The
  * tensor-core kernels wait on shared-memory barriers with an iteration

@@ -1,4 +1,5 @@
-"""Single-row cascade oracles: safe softmax of a row, variance, moment of inertia.
+"""Single-row cascade oracles: safe softmax of a row, variance, moment of
+inertia, layer normalisation.
 
 RedFuser episode transcript, cue 47: the paper measures safe softmax on rows
 of 1K to 8K elements at several fusion levels, and also runs variance and
@@ -49,3 +50,16 @@ def moment_of_inertia(mass, pos):
     d = p - c[:, :, None]
     inertia = np.einsum("rn,rdn->r", m, d * d)
     return c, inertia
+
+
+def layer_norm(x, gamma, beta, eps):
+    """x [R, n], gamma/beta [n] -> y [R, n].
+
+    Pass 1: mean; pass 2: population variance; pass 3: y = (x - mean) /
+    sqrt(var + eps) * gamma + beta (bookshelf explainer, "Problem":
+    normalisation layers are cascaded reductions).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    mean, var = row_variance(x)
+    return ((x - mean[:, None]) / np.sqrt(var[:, None] + eps) * np.asarray(gamma, np.float64)
+            + np.asarray(beta, np.float64))

@@ -156,3 +156,15 @@ def test_row_cascade_validation(lib):
     assert moi(FAKE, FAKE, 4, 64, FAKE, NULL, 1, NULL) == 1
     assert moi(FAKE, FAKE, 4, 6, FAKE, FAKE, 1, NULL) == 2
     assert moi(FAKE, ODD, 4, 64, FAKE, FAKE, 1, NULL) == 3
+
+
+def test_layer_norm_validation(lib):
+    ln = lib.rf_layer_norm
+    args = lambda **o: [o.get("x", FAKE), FAKE, FAKE, o.get("R", 4), o.get("n", 64), F(o.get("eps", 1e-5)),
+                        FAKE, o.get("level", 1), o.get("work", NULL), NULL]
+    assert ln(*args(x=NULL)) == 1
+    assert ln(*args(eps=-1.0)) == 1
+    assert ln(*args(level=0)) == 1                    # unfused needs work
+    assert ln(*args(n=66)) == 2
+    assert ln(*args(n=8196)) == 2
+    assert ln(*args(x=ODD)) == 3

@@ -74,3 +74,18 @@ def test_moment_of_inertia_parallel_axis_and_brute_force():
         # parallel-axis theorem: about the origin = about the centre + M |c|^2
         about_origin = sum(mass[r][i] * sum(pos[r][a][i] ** 2 for a in range(3)) for i in range(n))
         assert about_origin == pytest.approx(inertia[r] + M * sum(v * v for v in cx), rel=1e-12)
+
+
+def test_layer_norm_matches_torch_and_closed_form():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 777)) * 3 + 1
+    g = rng.standard_normal(777)
+    b = rng.standard_normal(777)
+    y = rc.layer_norm(x, g, b, 1e-5)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (777,), torch.from_numpy(g),
+                                         torch.from_numpy(b), 1e-5).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-12)
+    # with unit gain and zero bias every row has mean 0 and variance var/(var+eps)
+    z = rc.layer_norm(x, np.ones(777), np.zeros(777), 0.0)
+    np.testing.assert_allclose(z.mean(axis=1), 0.0, atol=1e-12)
+    np.testing.assert_allclose(z.var(axis=1), 1.0, rtol=1e-12)

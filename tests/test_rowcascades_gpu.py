@@ -131,3 +131,19 @@ def test_benchmark_sizes_sampled(rf, level):
     assert np.all(np.abs(f64(var[rows]) - rv) <= 2e-3 * rv + 1e-6)
     del x, y, xv
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("level", LEVELS)
+@pytest.mark.parametrize("n", [4, 1000, 4096, 8192])
+def test_layer_norm(rf, level, n):
+    g = torch.Generator().manual_seed(300 + n + level)
+    x = torch.randn(11, n, generator=g) * 3 + 2
+    gamma = torch.randn(n, generator=g)
+    beta = torch.randn(n, generator=g)
+    y = torch.empty(11, n, device="cuda")
+    work = torch.empty(22, device="cuda") if level == 0 else None
+    rf.rf_layer_norm(x.cuda(), gamma.cuda(), beta.cuda(), 1e-5, y, level, work)
+    torch.cuda.synchronize()
+    ref = rc.layer_norm(x.numpy(), gamma.numpy(), beta.numpy(), 1e-5)
+    # normalised values are O(1): relative bound plus a small absolute term
+    assert np.all(np.abs(f64(y) - ref) <= 2e-3 * np.abs(ref) + 1e-4), np.abs(f64(y) - ref).max()

@@ -324,6 +324,42 @@ def roofline(bound, achieved, peak, unit, traffic):
             "frac": round(achieved / peak, 4), "traffic": traffic}
 
 
+def decode_ablation(torch, rf, peaks, q, K, V, scale):
+    """Incremental vs non-incremental split-KV decode on the headline inputs,
+    for every segment count S: time of the segment-state kernel alone."""
+    R, L, D = K.shape
+    kv_bytes = 2 * R * L * D * 2
+    res = {}
+    for S in (1, 2, 4, 8, 16, 32, 64):
+        sm = torch.empty(R, S, device="cuda")
+        sl = torch.empty(R, S, device="cuda")
+        sa = torch.empty(R, S, D, device="cuda")
+        row = {}
+        for name, fn in (("incremental", rf.rf_attn_decode_split),
+                         ("non_incremental", rf.rf_attn_decode_split_twopass)):
+            try:
+                for _ in range(2):
+                    fn(q, K, V, S, scale, sm, sl, sa)
+            except rf.RFError as e:
+                row[name] = {"unsupported": str(e)}
+                continue
+            a, b = _events(torch, 2)
+            a.record()
+            for _ in range(5):
+                fn(q, K, V, S, scale, sm, sl, sa)
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / 5
+            gbs = kv_bytes / (ms * 1e-3) / 1e9
+            row[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                         "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        res[f"S{S}"] = row
+    res["workload"] = ("segment-state kernel only, B=32 H=32 L=32768 D=128 bf16; the "
+                       "non-incremental kernel keeps a segment's scores in shared memory "
+                       "(segments of at most 16384 keys)")
+    return res
+
+
 def path_single_row(torch, rf, peaks):
     import synthetic_inputs as si
     cfg = si.FULL["decode_f32"]
@@ -513,7 +549,10 @@ def run_rf(args):
                "quant": lambda: path_quant(torch, rf, peaks),
                "gemm": lambda: path_gemm(torch, rf, peaks),
                "prefill": lambda: path_prefill(torch, rf, peaks),
-               "rows": lambda: path_row_cascades(torch, rf, peaks)}
+               "rows": lambda: path_row_cascades(torch, rf, peaks),
+               "ablation": lambda: decode_ablation(
+                   torch, rf, peaks, *si.decode_inputs(1024, 32768, 128, torch.bfloat16, seed=2,
+                                                       device="cuda"), si.decode_scale(128))}
         print(json.dumps({args.only: fns[args.only]()}), flush=True)
         return
     B, H, L, D = DECODE["B"], DECODE["H"], DECODE["L"], DECODE["D"]
@@ -598,6 +637,8 @@ def run_rf(args):
 
     paths = {}
     if world == 1 and not args.decode_only:
+        paths["decode_incremental_vs_non_incremental"] = decode_ablation(torch, rf, peaks, q, K, V,
+                                                                         scale)
         del q, K, V
         torch.cuda.empty_cache()
         for name, fn in (("single_row_decode_f32", lambda: path_single_row(torch, rf, peaks)),
@@ -690,7 +731,8 @@ def main():
                     help="decode rows instead of B*H=1024 (small cases for ncu captures)")
     ap.add_argument("--decode-only", action="store_true", help="skip the other cascades")
     ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm",
-                                       "prefill", "rows"], help="time one other cascade alone")
+                                       "prefill", "rows", "ablation"],
+                    help="time one other cascade alone")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work")

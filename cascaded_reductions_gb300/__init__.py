@@ -46,6 +46,7 @@ _SIGNATURES = {
     "rf_row_variance": (_I, [_P, _I, _I, _P, _P, _I, _P]),
     "rf_moment_of_inertia": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
     "rf_layer_norm": (_I, [_P, _P, _P, _I, _I, _F, _P, _I, _P, _P]),
+    "rf_attn_decode_split_twopass": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
 }
 
 
@@ -124,6 +125,22 @@ def rf_attn_decode_split(q, k, v, S, scale, seg_m, seg_l, seg_acc, stream=None):
     _check(_lib.rf_attn_decode_split(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale),
                                      _dtype_code(k.dtype), _ptr(seg_m), _ptr(seg_l), _ptr(seg_acc),
                                      _stream(stream)), "rf_attn_decode_split")
+
+
+def rf_attn_decode_split_twopass(q, k, v, S, scale, seg_m, seg_l, seg_acc, stream=None):
+    """Non-incremental split-KV decode: same arguments and outputs as
+    rf_attn_decode_split; segments of at most 16384 keys."""
+    R, L, D = k.shape
+    _need(q, k.dtype, "q", (R, D))
+    _need(k, k.dtype, "k")
+    _need(v, k.dtype, "v", (R, L, D))
+    _need(seg_m, torch.float32, "seg_m", (R, S))
+    _need(seg_l, torch.float32, "seg_l", (R, S))
+    _need(seg_acc, torch.float32, "seg_acc", (R, S, D))
+    _check(_lib.rf_attn_decode_split_twopass(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale),
+                                             _dtype_code(k.dtype), _ptr(seg_m), _ptr(seg_l),
+                                             _ptr(seg_acc), _stream(stream)),
+           "rf_attn_decode_split_twopass")
 
 
 def rf_state_merge(seg_m, seg_l, seg_acc, out, lse=None, stream=None):

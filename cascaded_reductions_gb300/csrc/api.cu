@@ -41,6 +41,20 @@ rf_status rf_attn_decode_split(const void* q, const void* k, const void* v, int 
                                  as_stream(stream));
 }
 
+rf_status rf_attn_decode_split_twopass(const void* q, const void* k, const void* v, int R, int L,
+                                       int D, int S, float scale, int dtype, float* seg_m,
+                                       float* seg_l, float* seg_acc, void* stream) {
+  if (!q || !k || !v || !seg_m || !seg_l || !seg_acc) return RF_ERR_INVALID_ARG;
+  if (R <= 0 || L <= 0 || D <= 0 || S < 1 || !isfinite(scale)) return RF_ERR_INVALID_ARG;
+  if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (!((dtype == RF_F32 && D == 64) || (dtype == RF_BF16 && D == 128))) return RF_ERR_UNSUPPORTED;
+  if ((long long)R * S > 0x7fffffffLL) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(q) || !rf::aligned16(k) || !rf::aligned16(v) || !rf::aligned16(seg_acc))
+    return RF_ERR_MISALIGNED;
+  return rf::launch_decode_twopass(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                                   as_stream(stream));
+}
+
 rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc, int R,
                          int S, int D, void* out, int out_dtype, float* lse, void* stream) {
   if (!seg_m || !seg_l || !seg_acc || !out) return RF_ERR_INVALID_ARG;

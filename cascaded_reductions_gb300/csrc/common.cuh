@@ -48,6 +48,37 @@ __device__ __forceinline__ float group_sum(float x) {
   return x;
 }
 
+// A 16-byte chunk of a key/value row as floats: 4 fp32 or 8 bf16 values.
+template <typename T>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+};
+
+struct Bf16Tag {};
+template <>
+struct Chunk<Bf16Tag> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
+    f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
+    f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+  }
+};
+
+// Rescale reference for a running max that may still be -inf (no key seen):
+// exp2(x - ref) is then 0 for x = -inf and the state stays the identity.
+__device__ __forceinline__ float ref_of(float m) { return m == -INFINITY ? 0.f : m; }
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline rf_status launch_status() {
@@ -60,6 +91,9 @@ inline rf_status launch_status() {
 rf_status launch_decode_split(const void* q, const void* k, const void* v, int R, int L, int D,
                               int S, float scale, int dtype, float* seg_m, float* seg_l,
                               float* seg_acc, cudaStream_t st);
+rf_status launch_decode_twopass(const void* q, const void* k, const void* v, int R, int L, int D,
+                                int S, float scale, int dtype, float* seg_m, float* seg_l,
+                                float* seg_acc, cudaStream_t st);
 rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc, int R,
                              int S, int D, void* out, int out_dtype, float* lse, cudaStream_t st);
 rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int renormalize,

@@ -31,38 +31,6 @@
 namespace rf {
 namespace {
 
-template <typename T>
-struct Chunk;
-
-// 16 bytes = 4 fp32 values
-template <>
-struct Chunk<float> {
-  static constexpr int N = 4;
-  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
-    f[0] = __uint_as_float(u.x);
-    f[1] = __uint_as_float(u.y);
-    f[2] = __uint_as_float(u.z);
-    f[3] = __uint_as_float(u.w);
-  }
-};
-
-// 16 bytes = 8 bf16 values
-struct Bf16Tag {};
-template <>
-struct Chunk<Bf16Tag> {
-  static constexpr int N = 8;
-  __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
-    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
-    f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
-    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z);
-    f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
-  }
-};
-
-// Rescale reference for a running max that may still be -inf (no key seen):
-// exp2(x - ref) is then 0 for x = -inf and the state stays the identity.
-__device__ __forceinline__ float ref_of(float m) { return m == -INFINITY ? 0.f : m; }
-
 template <typename T, int WARPS, int U>
 __global__ void __launch_bounds__(WARPS * 32)
 decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,

@@ -86,6 +86,21 @@ rf_status rf_attn_decode_split(const void* q, const void* k, const void* v,
                                void* stream);
 
 /*
+ * rf_attn_decode_split_twopass -- the non-incremental counterpart of
+ * rf_attn_decode_split, for the incremental vs non-incremental comparison of
+ * transcript cue 45 (the non-incremental form fits only short per-block
+ * sequences).  Same arguments and the same segment states out; each CTA
+ * first computes and keeps every score of its segment in shared memory and
+ * reduces their max, then accumulates l and acc against that final max with
+ * no rescaling.  Segments (ceil(L/S) keys) must not exceed 16384 keys:
+ * RF_ERR_UNSUPPORTED otherwise.
+ */
+rf_status rf_attn_decode_split_twopass(const void* q, const void* k, const void* v,
+                                       int R, int L, int D, int S, float scale, int dtype,
+                                       float* seg_m, float* seg_l, float* seg_acc,
+                                       void* stream);
+
+/*
  * rf_state_merge -- combine the S segment states of each row and normalise
  * (transcript cue 21: two partial states, each with its own max, combine with
  * the same rescaling; viz page widget "Merging partial states across blocks").

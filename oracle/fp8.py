@@ -118,3 +118,43 @@ def quant_gemm(x, wq, sw):
     """The whole cascade: absmax quant of X, then the scaled FP8 GEMM."""
     xq, sx = absmax_quant(x)
     return xq, sx, scaled_gemm(xq, sx, wq, sw)
+
+
+def incremental_quant_gemm(x, wq, sw, tile_k=128):
+    """The incremental form of the abs-max -> quantise -> GEMM cascade.
+
+    RedFuser episode transcript, cue 33: the abs-max enters the GEMM as one
+    multiplicative factor, so when the running abs-max grows the running
+    accumulator is multiplied by the old abs-max over the new one.  Written out
+    per row, K-tile by K-tile (tiles of ``tile_k`` columns, in order):
+
+      a' = max(a, max over the tile of |x|);   s' = fp32(a' / 448)
+      if a > 0 and a' > a:   acc *= s / s'      (= a / a', the rescale)
+      codes = e4m3(fp32(x_tile / s'))           (s' = 0: zero codes)
+      acc += codes . Wq_tile^T                  (float64)
+
+    and finally Y = acc * s_final * sw.  The same quantisation rules as
+    ``absmax_quant`` apply to every tile; only the scale differs (the running
+    one instead of the whole row's).  Returns (Y float64 [M, N], s_final
+    float32 [M]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    M, K = x.shape
+    B = e4m3_decode(wq)
+    acc = np.zeros((M, B.shape[0]))
+    a = np.zeros(M)
+    s = np.zeros(M, dtype=np.float32)
+    for k0 in range(0, K, tile_k):
+        xt = x[:, k0:k0 + tile_k]
+        a_new = np.maximum(a, np.abs(xt).max(axis=1))
+        s_new = (a_new / E4M3_MAX).astype(np.float32)
+        grow = (a > 0) & (a_new > a)
+        factor = np.where(grow, s.astype(np.float64) / np.where(grow, s_new.astype(np.float64), 1.0), 1.0)
+        acc *= factor[:, None]
+        zero = s_new == 0
+        denom = np.where(zero, 1.0, s_new.astype(np.float64))
+        codes = e4m3_encode((xt / denom[:, None]).astype(np.float32))
+        codes[zero, :] = 0
+        acc += e4m3_decode(codes) @ B[:, k0:k0 + tile_k].T
+        a, s = a_new, s_new
+    return acc * s.astype(np.float64)[:, None] * np.asarray(sw, np.float64)[None, :], s

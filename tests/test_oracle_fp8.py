@@ -208,3 +208,48 @@ def test_quant_scale_and_quotient_are_correctly_rounded_fp32():
             v = _nearest_f32(abs(xv) / s)
             v = np.float32(-v) if xv < 0 else np.float32(v)
             assert xq[r, kk] == _nearest_code_brute(v)
+
+
+def test_incremental_equals_two_phase_when_the_max_comes_first():
+    """If every row's abs-max sits in the first K-tile the running scale never
+    changes: the incremental form uses the final scale throughout and must give
+    the two-phase result."""
+    rng = np.random.default_rng(7)
+    M, K, N = 6, 512, 40
+    x = bf16.decode(bf16.encode_from_f32(rng.standard_normal((M, K)).astype(np.float32)))
+    x[:, 3] = 50.0 * np.sign(rng.standard_normal(M))
+    wq = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
+    sw = rng.uniform(0.5, 2, N).astype(np.float32)
+    y_inc, s_inc = fp8.incremental_quant_gemm(x, wq, sw)
+    xq, sx = fp8.absmax_quant(x)
+    np.testing.assert_array_equal(s_inc, sx)
+    np.testing.assert_allclose(y_inc, fp8.scaled_gemm(xq, sx, wq, sw), rtol=1e-12, atol=1e-12)
+
+
+def test_incremental_rescale_closed_form():
+    """Row [112, 896] in two tiles of one column: tile 0 has scale 112/448 = 1/4
+    and code 448; tile 1 raises the scale to 2 (code 448) and rescales the
+    accumulator by (1/4)/2.  Every scale is a power of two and every value lies
+    on the e4m3 grid, so with w = [1, 0.5]: Y = 112 * 1 + 896 * 0.5 exactly."""
+    x = np.array([[112.0, 896.0]])
+    wq = np.array([[0x38, 0x30]], dtype=np.uint8)     # 1.0 and 0.5
+    y, s = fp8.incremental_quant_gemm(x, wq, np.ones(1, np.float32), tile_k=1)
+    assert s[0] == np.float32(2.0)
+    assert y[0, 0] == 112.0 * 1.0 + 896.0 * 0.5
+
+
+def test_incremental_zero_prefix_and_error_bound():
+    rng = np.random.default_rng(8)
+    M, K, N = 4, 384, 16
+    x = bf16.decode(bf16.encode_from_f32(rng.standard_normal((M, K)).astype(np.float32)))
+    x[0, :200] = 0.0                                  # scale 0 for the first tile, then grows
+    x[1] = 0.0                                        # all-zero row
+    wq = rng.integers(0, 0x7E, (N, K)).astype(np.uint8)
+    sw = np.ones(N, np.float32)
+    y, s = fp8.incremental_quant_gemm(x, wq, sw)
+    assert s[1] == 0 and np.all(y[1] == 0)
+    # each tile is quantised at most as coarsely as with the final scale, so the
+    # result stays within the e4m3 rounding bound of the exact product
+    exact = x @ fp8.e4m3_decode(wq).T
+    bound = (np.abs(x) * 2.0 ** -4).sum(axis=1)[:, None] * np.abs(fp8.e4m3_decode(wq)).max()
+    assert np.all(np.abs(y - exact) <= bound + 1e-9)

@@ -47,6 +47,7 @@ _SIGNATURES = {
     "rf_moment_of_inertia": (_I, [_P, _P, _I, _I, _P, _P, _I, _P]),
     "rf_layer_norm": (_I, [_P, _P, _P, _I, _I, _F, _P, _I, _P, _P]),
     "rf_attn_decode_split_twopass": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
+    "rf_incremental_quant_fp8_gemm": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P]),
 }
 
 
@@ -278,6 +279,21 @@ def rf_layer_norm(x, gamma, beta, eps, y, level, work=None, stream=None):
         _need(work, torch.float32, "work", (2 * R,))
     _check(_lib.rf_layer_norm(_ptr(x), _ptr(gamma), _ptr(beta), R, n, float(eps), _ptr(y),
                               int(level), _ptr(work), _stream(stream)), "rf_layer_norm")
+
+
+def rf_incremental_quant_fp8_gemm(x, wq, sw, y, sx_final=None, stream=None):
+    """x [M, K] bf16, wq [N, K] uint8 e4m3, sw [N] -> y [M, N] bf16, sx_final [M] (optional)."""
+    M, K = x.shape
+    N = wq.shape[0]
+    _need(x, torch.bfloat16, "x")
+    _need(wq, torch.uint8, "wq", (N, K))
+    _need(sw, torch.float32, "sw", (N,))
+    _need(y, torch.bfloat16, "y", (M, N))
+    if sx_final is not None:
+        _need(sx_final, torch.float32, "sx_final", (M,))
+    _check(_lib.rf_incremental_quant_fp8_gemm(_ptr(x), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
+                                              _ptr(sx_final), _stream(stream)),
+           "rf_incremental_quant_fp8_gemm")
 
 
 def rf_device_error(stream=None):

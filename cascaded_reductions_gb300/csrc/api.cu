@@ -171,6 +171,17 @@ rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, i
   return rf::launch_layer_norm(x, gamma, beta, R, n, eps, y, level, work, as_stream(stream));
 }
 
+rf_status rf_incremental_quant_fp8_gemm(const void* x, int M, int K, const uint8_t* wq,
+                                        const float* sw, int N, void* y, float* sx_final,
+                                        void* stream) {
+  if (!x || !wq || !sw || !y) return RF_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return RF_ERR_INVALID_ARG;
+  if (M % 128 != 0 || N % 512 != 0 || K % 128 != 0) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(x) || !rf::aligned16(wq) || !rf::aligned16(y) || !rf::aligned16(sw))
+    return RF_ERR_MISALIGNED;
+  return rf::launch_fp8_incremental(x, wq, sw, M, N, K, y, sx_final, as_stream(stream));
+}
+
 rf_status rf_device_error(int* status, void* stream) {
   if (!status) return RF_ERR_INVALID_ARG;
   return rf::read_device_error(status, as_stream(stream));

@@ -112,6 +112,9 @@ rf_status launch_moment_of_inertia(const float* mass, const float* pos, int R, i
                                    float* center, float* inertia, int level, cudaStream_t st);
 rf_status launch_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
                             float eps, float* y, int level, float* work, cudaStream_t st);
+rf_status launch_fp8_incremental(const void* x, const uint8_t* wq, const float* sw, int M, int N,
+                                 int K, void* y, float* sx_final, cudaStream_t st);
+rf_status fp8_incremental_take_status(int* status);
 rf_status read_device_error(int* status, cudaStream_t st);
 // read and clear the bounded-wait status word of each tensor-core kernel file
 rf_status gemm_take_status(int* status);

@@ -24,6 +24,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "e4m3.cuh"
 
 namespace rf {
 namespace {
@@ -43,41 +44,6 @@ __device__ __forceinline__ uint32_t absmax8(const uint4& u, uint32_t a) {
 __device__ __forceinline__ float absmax_value(uint32_t pair) {
   return fmaxf(bf16_lo(pair), bf16_hi(pair));
 }
-
-// two floats -> two e4m3 codes (x0 in the low byte), RNE, saturating
-__device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
-  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-}
-
-// correctly rounded x / s from r = RN(1/s) (see the file comment); the sign
-// of a zero x is kept
-__device__ __forceinline__ float quotient(float x, float s, float r) {
-  float q = x * r;
-  q = fmaf(fmaf(-q, s, x), r, q);
-  q = fmaf(fmaf(-q, s, x), r, q);
-  return copysignf(q, x);
-}
-
-__device__ __forceinline__ uint2 encode8(const uint4& u, float s, float r) {
-  const uint32_t c0 = e4m3x2(quotient(bf16_lo(u.x), s, r), quotient(bf16_hi(u.x), s, r));
-  const uint32_t c1 = e4m3x2(quotient(bf16_lo(u.y), s, r), quotient(bf16_hi(u.y), s, r));
-  const uint32_t c2 = e4m3x2(quotient(bf16_lo(u.z), s, r), quotient(bf16_hi(u.z), s, r));
-  const uint32_t c3 = e4m3x2(quotient(bf16_lo(u.w), s, r), quotient(bf16_hi(u.w), s, r));
-  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
-}
-
-// rows with a tiny (or zero) scale: IEEE division per element, or zero codes
-__device__ __noinline__ uint2 encode8_exact(uint4 u, float s) {
-  if (s == 0.f) return make_uint2(0u, 0u);
-  const uint32_t c0 = e4m3x2(__fdiv_rn(bf16_lo(u.x), s), __fdiv_rn(bf16_hi(u.x), s));
-  const uint32_t c1 = e4m3x2(__fdiv_rn(bf16_lo(u.y), s), __fdiv_rn(bf16_hi(u.y), s));
-  const uint32_t c2 = e4m3x2(__fdiv_rn(bf16_lo(u.z), s), __fdiv_rn(bf16_hi(u.z), s));
-  const uint32_t c3 = e4m3x2(__fdiv_rn(bf16_lo(u.w), s), __fdiv_rn(bf16_hi(u.w), s));
-  return make_uint2(c0 | (c1 << 16), c2 | (c3 << 16));
-}
-
-// the reciprocal-and-correction path is valid for scales of 2^-90 and up
-__device__ __forceinline__ bool fast_scale(float s) { return s >= 0x1p-90f; }
 
 template <int THREADS>
 __device__ __forceinline__ float block_max(float a, float* red) {

@@ -207,6 +207,25 @@ rf_status rf_attn_decode_noalloc(const void* q, const void* k, const void* v,
                                  int R, int L, int D, int S, float scale, int dtype,
                                  void* out, int out_dtype, float* lse, void* stream);
 
+/*
+ * rf_incremental_quant_fp8_gemm -- the incremental form of the FP8 cascade in
+ * one kernel (transcript cue 33: when the running abs-max grows, multiply the
+ * running accumulator by the old abs-max over the new one).  Per row and
+ * K-tile of 128 columns, in order: a' = max(a, tile max |x|), s' = fp32(a' /
+ * 448); if the scale grew, acc *= s / s'; the tile is quantised with s' (the
+ * same rounding as rf_absmax_quant_e4m3) and accumulated on the FP8 tensor
+ * cores; Y = bf16(acc * s_final * sw).  The codes of early tiles use the
+ * running scale, so Y differs from rf_absmax_quant_fp8_gemm's (it is a
+ * different quantisation of X, at least as fine); no Xq is written.
+ *   x [M, K] bf16;  wq [N, K] e4m3;  sw [N] fp32;  y [M, N] bf16 out
+ *   sx_final [M] fp32 out (the final per-row scale), may be NULL
+ * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
+ * RF_ERR_UNSUPPORTED unless M % 128 == 0, N % 512 == 0 and K % 128 == 0.
+ */
+rf_status rf_incremental_quant_fp8_gemm(const void* x, int M, int K, const uint8_t* wq,
+                                        const float* sw, int N, void* y, float* sx_final,
+                                        void* stream);
+
 /* Phase 1 of rf_absmax_quant_fp8_gemm alone (same arguments and rules;
  * any K % 8 == 0 is supported). */
 rf_status rf_absmax_quant_e4m3(const void* x, int M, int K, uint8_t* xq, float* sx,

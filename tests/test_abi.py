@@ -168,3 +168,14 @@ def test_layer_norm_validation(lib):
     assert ln(*args(n=66)) == 2
     assert ln(*args(n=8196)) == 2
     assert ln(*args(x=ODD)) == 3
+
+
+def test_incremental_fp8_validation(lib):
+    f = lib.rf_incremental_quant_fp8_gemm
+    args = lambda **o: [o.get("x", FAKE), o.get("M", 128), o.get("K", 256), FAKE, FAKE,
+                        o.get("N", 512), FAKE, NULL, NULL]
+    assert f(*args(x=NULL)) == 1
+    assert f(*args(M=0)) == 1
+    assert f(*args(N=256)) == 2
+    assert f(*args(K=100)) == 2
+    assert f(*args(x=ODD)) == 3

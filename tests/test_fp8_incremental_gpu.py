@@ -1,0 +1,94 @@
+"""Parity of the incremental FP8 quantise-in-GEMM (rf_incremental_quant_fp8_gemm)
+with the oracle's incremental form, through the C ABI: Y within the bf16
+tolerance, the final per-row scales bit-exact.
+
+Cases: one K-tile; several tiles where the abs-max grows (outliers placed
+late, so the accumulator is rescaled); rows whose abs-max comes first (then
+the result equals the two-phase cascade's); zero rows and a zero prefix; and
+the full workload [4096 x 7168] x [4096 x 7168] on sampled rows."""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close_bf16, f64
+from oracle import bf16 as obf16
+from oracle import fp8 as ofp8
+import synthetic_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def rf():
+    import cascaded_reductions_gb300 as m
+    return m
+
+
+def run(rf, x, wq, sw):
+    M, K = x.shape
+    N = wq.shape[0]
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    sx = torch.empty(M, device="cuda")
+    rf.rf_incremental_quant_fp8_gemm(x.cuda(), wq.cuda(), sw.cuda(), y, sx)
+    torch.cuda.synchronize()
+    assert rf.rf_device_error() == 0
+    return f64(y), sx.cpu().numpy()
+
+
+def check(rf, x, wq, sw, what, rows=None):
+    gy, gs = run(rf, x, wq, sw)
+    xs = x if rows is None else x[rows]
+    ry, rs = ofp8.incremental_quant_gemm(obf16.decode(xs.view(torch.int16).numpy()), wq.numpy(),
+                                         sw.numpy())
+    if rows is not None:
+        gy, gs = gy[rows], gs[rows]
+    assert np.array_equal(gs, rs), f"{what}: final scales differ"
+    assert_close_bf16(gy, ry, what)
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 128, 512), (256, 1024, 512), (128, 2048, 1024)])
+def test_shapes(rf, M, K, N):
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=M + K + N)
+    check(rf, x, wq, sw, f"M={M} K={K} N={N}")
+
+
+def test_growing_abs_max_rescales(rf):
+    M, K, N = 128, 1024, 512
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=21)
+    xf = x.float()
+    # the row maximum grows tile after tile: each later tile gets a larger outlier
+    for t in range(K // 128):
+        xf[:, t * 128 + 5] = 2.0 * (t + 1) * torch.sign(xf[:, t * 128 + 5] + 0.5)
+    check(rf, xf.to(torch.bfloat16), wq, sw, "growing")
+
+
+def test_max_first_equals_two_phase(rf):
+    M, K, N = 128, 1024, 512
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=22)
+    xf = x.float()
+    xf[:, 0] = 60.0
+    x = xf.to(torch.bfloat16)
+    gy, gs = run(rf, x, wq, sw)
+    xq, sx, y2 = rf.absmax_quant_fp8_gemm(x.cuda(), wq.cuda(), sw.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(gs, sx.cpu().numpy())
+    assert_close_bf16(gy, f64(y2), "vs two-phase")
+
+
+def test_zero_rows_and_zero_prefix(rf):
+    M, K, N = 128, 768, 512
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=23)
+    xf = x.float()
+    xf[0] = 0.0
+    xf[1, :300] = 0.0
+    check(rf, xf.to(torch.bfloat16), wq, sw, "zeros")
+    gy, gs = run(rf, xf.to(torch.bfloat16), wq, sw)
+    assert gs[0] == 0 and np.all(gy[0] == 0)
+
+
+def test_full_size_sampled_rows(rf):
+    cfg = si.FULL["quant_gemm"]
+    x, wq, sw = si.quant_gemm_inputs(cfg["M"], cfg["K"], cfg["N"], seed=si.SEEDS["quant_gemm"])
+    rows = sorted(set(np.random.default_rng(0).choice(cfg["M"], 48, replace=False).tolist() + [0, 4095]))
+    check(rf, x, wq, sw, "4096x7168x4096", rows=rows)

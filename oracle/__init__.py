@@ -22,6 +22,8 @@ float64 (numpy), exactly as the pages state the stages:
   encode, then the GEMM sum (transcript cue 33).
 * single-row cascades -- safe softmax of a row, variance, moment of inertia
   (transcript cue 47).
+* multi-latent attention decode -- the attention cascade with every query
+  head reading one shared latent cache (transcript cues 41 and 55).
 
 Every floating-point step is float64 unless the step itself is a rounding to a
 narrower format the method fixes (fp32 scale and fp32 quotient before the e4m3
@@ -34,4 +36,4 @@ scaled-dot-product attention, torch's own float8/bfloat16 casts), the e4m3
 definition checked exhaustively, and brute force on tiny inputs.
 """
 
-from . import attention, routing, fp8, bf16, rowcascades  # noqa: F401
+from . import attention, routing, fp8, bf16, rowcascades, mla  # noqa: F401

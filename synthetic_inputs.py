@@ -20,7 +20,11 @@ in the order listed; fp32 draws are cast to bf16 where the workload is bf16):
   column scale sw_n = fp32(max_k |W_kn| / 448) and codes from torch's own
   float8_e4m3fn cast of W / sw, stored transposed as Wq [N, K] (K contiguous);
 * causal prefill (bf16, B=4, H=32, N=8192, D=128): Q, K, V ~ N(0,1), seed 5,
-  scale 1/sqrt(128).
+  scale 1/sqrt(128);
+* multi-latent attention decode (bf16, B=64 sequences, H=16 query heads,
+  L=32768 keys, latent width Dk=576 = 512 + 64 rotary, value width Dv=512):
+  q [B, H, Dk], C [B, L, Dk] ~ N(0,1), seed 6, scale 1/sqrt(192) (the
+  128 + 64 query/key head width the latent form stands in for).
 
 Smaller parity cases use the same recipe with smaller sizes.
 """
@@ -30,7 +34,7 @@ import math
 import torch
 
 SEEDS = {"decode_f32": 1, "decode_bf16": 2, "route_256": 3, "route_64": 33,
-         "quant_gemm": 4, "prefill": 5}
+         "quant_gemm": 4, "prefill": 5, "mla": 6}
 
 FULL = {
     "decode_f32": dict(R=1, L=4096, D=64),
@@ -39,6 +43,7 @@ FULL = {
     "route_64": dict(T=65536, E=64, k=2),
     "quant_gemm": dict(M=4096, K=7168, N=4096),
     "prefill": dict(B=4, H=32, N=8192, D=128),
+    "mla": dict(B=64, H=16, L=32768, Dk=576, Dv=512),
 }
 
 
@@ -92,3 +97,19 @@ def prefill_inputs(B, H, N, D, seed=5, device="cpu"):
         return tuple(torch.randn(B, H, N, D, generator=g).to(torch.bfloat16) for _ in range(3))
     return tuple(torch.randn(B, H, N, D, generator=g, device=device, dtype=torch.bfloat16)
                  for _ in range(3))
+
+
+def mla_inputs(B, H, L, Dk=576, seed=6, device="cpu"):
+    """q [B, H, Dk], C [B, L, Dk] bf16 ~ N(0,1) (query heads, shared latent cache)."""
+    g = _gen(seed, device)
+    if device == "cpu":
+        q = torch.randn(B, H, Dk, generator=g).to(torch.bfloat16)
+        C = torch.randn(B, L, Dk, generator=g).to(torch.bfloat16)
+    else:
+        q = torch.randn(B, H, Dk, generator=g, device=device, dtype=torch.bfloat16)
+        C = torch.randn(B, L, Dk, generator=g, device=device, dtype=torch.bfloat16)
+    return q, C
+
+
+def mla_scale():
+    return 1.0 / math.sqrt(192)

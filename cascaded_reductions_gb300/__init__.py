@@ -48,6 +48,7 @@ _SIGNATURES = {
     "rf_layer_norm": (_I, [_P, _P, _P, _I, _I, _F, _P, _I, _P, _P]),
     "rf_attn_decode_split_twopass": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "rf_incremental_quant_fp8_gemm": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P]),
+    "rf_mla_decode_split": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
 }
 
 
@@ -142,6 +143,22 @@ def rf_attn_decode_split_twopass(q, k, v, S, scale, seg_m, seg_l, seg_acc, strea
                                              _dtype_code(k.dtype), _ptr(seg_m), _ptr(seg_l),
                                              _ptr(seg_acc), _stream(stream)),
            "rf_attn_decode_split_twopass")
+
+
+def rf_mla_decode_split(q, c, S, scale, seg_m, seg_l, seg_acc, stream=None):
+    """q [B, H, 576], c [B, L, 576] bf16 (shared latent cache) -> seg_m/seg_l [B, H, S],
+    seg_acc [B, H, S, 512] fp32."""
+    B, H, Dk = q.shape
+    L = c.shape[1]
+    Dv = seg_acc.shape[-1]
+    _need(q, torch.bfloat16, "q")
+    _need(c, torch.bfloat16, "c", (B, L, Dk))
+    _need(seg_m, torch.float32, "seg_m", (B, H, S))
+    _need(seg_l, torch.float32, "seg_l", (B, H, S))
+    _need(seg_acc, torch.float32, "seg_acc", (B, H, S, Dv))
+    _check(_lib.rf_mla_decode_split(_ptr(q), _ptr(c), B, H, L, Dk, Dv, S, float(scale),
+                                    _ptr(seg_m), _ptr(seg_l), _ptr(seg_acc), _stream(stream)),
+           "rf_mla_decode_split")
 
 
 def rf_state_merge(seg_m, seg_l, seg_acc, out, lse=None, stream=None):
@@ -319,6 +336,26 @@ def attn_decode(q, k, v, S, scale, out_dtype=None, return_states=False, stream=N
     lse = torch.empty(R, device=dev, dtype=torch.float32)
     rf_attn_decode_split(q, k, v, S, scale, seg_m, seg_l, seg_acc, stream)
     rf_state_merge(seg_m, seg_l, seg_acc, out, lse, stream)
+    if return_states:
+        return out, lse, (seg_m, seg_l, seg_acc)
+    return out, lse
+
+
+def mla_decode(q, c, S, scale, dv=512, return_states=False, stream=None):
+    """MLA split decode: rf_mla_decode_split then rf_state_merge.
+
+    q [B, H, 576], c [B, L, 576] bf16; returns out [B, H, dv] bf16 and lse [B, H]
+    (and the segment states if ``return_states``)."""
+    B, H, _ = q.shape
+    dev = q.device
+    seg_m = torch.empty(B, H, S, device=dev, dtype=torch.float32)
+    seg_l = torch.empty(B, H, S, device=dev, dtype=torch.float32)
+    seg_acc = torch.empty(B, H, S, dv, device=dev, dtype=torch.float32)
+    out = torch.empty(B, H, dv, device=dev, dtype=torch.bfloat16)
+    lse = torch.empty(B, H, device=dev, dtype=torch.float32)
+    rf_mla_decode_split(q, c, S, scale, seg_m, seg_l, seg_acc, stream)
+    rf_state_merge(seg_m.view(B * H, S), seg_l.view(B * H, S), seg_acc.view(B * H, S, dv),
+                   out.view(B * H, dv), lse.view(B * H), stream)
     if return_states:
         return out, lse, (seg_m, seg_l, seg_acc)
     return out, lse

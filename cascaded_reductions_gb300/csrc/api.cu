@@ -60,10 +60,21 @@ rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* se
   if (!seg_m || !seg_l || !seg_acc || !out) return RF_ERR_INVALID_ARG;
   if (R <= 0 || S <= 0 || D <= 0) return RF_ERR_INVALID_ARG;
   if (out_dtype != RF_F32 && out_dtype != RF_BF16) return RF_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return RF_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128 && D != 512) return RF_ERR_UNSUPPORTED;
   if (!rf::aligned16(seg_acc) || !rf::aligned16(out)) return RF_ERR_MISALIGNED;
   return rf::launch_state_merge(seg_m, seg_l, seg_acc, R, S, D, out, out_dtype, lse,
                                 as_stream(stream));
+}
+
+rf_status rf_mla_decode_split(const void* q, const void* c, int B, int H, int L, int Dk,
+                              int Dv, int S, float scale, float* seg_m, float* seg_l,
+                              float* seg_acc, void* stream) {
+  if (!q || !c || !seg_m || !seg_l || !seg_acc) return RF_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || L <= 0 || S < 1 || !isfinite(scale)) return RF_ERR_INVALID_ARG;
+  if (Dk != 576 || Dv != 512 || H % 16 != 0) return RF_ERR_UNSUPPORTED;
+  if ((long long)B * L >= (1ll << 31) || (long long)B * H >= (1ll << 31)) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(q) || !rf::aligned16(c) || !rf::aligned16(seg_acc)) return RF_ERR_MISALIGNED;
+  return rf::launch_mla_decode(q, c, B, H, L, S, scale, seg_m, seg_l, seg_acc, as_stream(stream));
 }
 
 rf_status rf_attn_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,

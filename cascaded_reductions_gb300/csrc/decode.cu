@@ -163,9 +163,9 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
   }
 }
 
-// One warp per row.  Lane j owns 4 consecutive elements of D (D = 128) or
-// lanes 0..15 own them (D = 64); the segment weights exp(m_s - M) are
-// computed by every lane from the (cached) seg_m row.
+// One warp per row.  Lane j owns 4 consecutive elements of every 128-wide
+// block of D (D = 128, 512), or lanes 0..15 own them (D = 64); the segment
+// weights exp(m_s - M) are computed by every lane from the (cached) seg_m row.
 template <int D, bool BF16_OUT>
 __global__ void __launch_bounds__(256)
 state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ seg_l,
@@ -186,27 +186,38 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
   for (int s = lane; s < S; s += 32) Lsum = fmaf(expf(mr[s] - ref), lr[s], Lsum);
   Lsum = group_sum<32>(Lsum);
 
-  constexpr int LANES = D / 4;
-  if (lane < LANES) {
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int V4 = D / 4;                     // float4s per state
+  constexpr int NB = V4 < 32 ? 1 : V4 / 32;     // float4s per lane
+  if (lane < V4) {
+    float4 A[NB];
+#pragma unroll
+    for (int i = 0; i < NB; ++i) A[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* ar = reinterpret_cast<const float4*>(seg_acc + (size_t)row * S * D) + lane;
     for (int s = 0; s < S; ++s) {
       const float f = expf(mr[s] - ref);
-      const float4 x = ar[(size_t)s * LANES];
-      A.x = fmaf(f, x.x, A.x);
-      A.y = fmaf(f, x.y, A.y);
-      A.z = fmaf(f, x.z, A.z);
-      A.w = fmaf(f, x.w, A.w);
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        const float4 x = ar[(size_t)s * V4 + 32 * i];
+        A[i].x = fmaf(f, x.x, A[i].x);
+        A[i].y = fmaf(f, x.y, A[i].y);
+        A[i].z = fmaf(f, x.z, A[i].z);
+        A[i].w = fmaf(f, x.w, A[i].w);
+      }
     }
     const float inv = 1.f / Lsum;
-    A.x *= inv; A.y *= inv; A.z *= inv; A.w *= inv;
-    if (BF16_OUT) {
-      uint2 p;
-      p.x = pack_bf16x2(A.x, A.y);
-      p.y = pack_bf16x2(A.z, A.w);
-      reinterpret_cast<uint2*>(out)[(size_t)row * LANES + lane] = p;
-    } else {
-      reinterpret_cast<float4*>(out)[(size_t)row * LANES + lane] = A;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) {
+      float4 a = A[i];
+      a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
+      const size_t o = (size_t)row * V4 + lane + 32 * i;
+      if (BF16_OUT) {
+        uint2 p;
+        p.x = pack_bf16x2(a.x, a.y);
+        p.y = pack_bf16x2(a.z, a.w);
+        reinterpret_cast<uint2*>(out)[o] = p;
+      } else {
+        reinterpret_cast<float4*>(out)[o] = a;
+      }
     }
   }
   if (lse != nullptr && lane == 0) lse[row] = M + logf(Lsum);
@@ -246,6 +257,9 @@ rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float
   } else if (D == 64) {
     if (bf) state_merge_kernel<64, true><<<grid, 256, 0, st>>>(seg_m, seg_l, seg_acc, R, S, out, lse);
     else state_merge_kernel<64, false><<<grid, 256, 0, st>>>(seg_m, seg_l, seg_acc, R, S, out, lse);
+  } else if (D == 512) {
+    if (bf) state_merge_kernel<512, true><<<grid, 256, 0, st>>>(seg_m, seg_l, seg_acc, R, S, out, lse);
+    else state_merge_kernel<512, false><<<grid, 256, 0, st>>>(seg_m, seg_l, seg_acc, R, S, out, lse);
   } else {
     return RF_ERR_UNSUPPORTED;
   }

@@ -108,16 +108,50 @@ rf_status rf_attn_decode_split_twopass(const void* q, const void* k, const void*
  *   l = sum_s w_s l_s;  acc = sum_s w_s acc_s;  out = acc / l;  lse = M + ln l.
  *
  *   seg_m, seg_l, seg_acc   as written by rf_attn_decode_split
- *   R, S, D                 rows, segments, head dim (D = 64 or 128)
+ *                           or rf_mla_decode_split
+ *   R, S, D                 rows, segments, value width (D = 64, 128 or 512)
  *   out        [R, D]       out_dtype out (RF_F32 or RF_BF16, round to nearest even)
  *   lse        [R]          fp32 out, may be NULL
  * Errors: RF_ERR_INVALID_ARG for null inputs/out, R, S, D <= 0;
- * RF_ERR_UNSUPPORTED for D not in {64, 128}.
+ * RF_ERR_UNSUPPORTED for D not in {64, 128, 512}.
  * A row whose S states are all identity states gives NaN (it had no keys).
  */
 rf_status rf_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc,
                          int R, int S, int D, void* out, int out_dtype, float* lse,
                          void* stream);
+
+/*
+ * rf_mla_decode_split -- multi-latent attention (MLA) decode, producer of
+ * segment states (transcript cue 41: the MLA workload, compared with
+ * DeepSeek's FlashMLA; cue 55: decode shapes, one query row; cue 39: the
+ * Multi-Segment split).  Every query head of a sequence reads the same latent
+ * cache row c_j [Dk]; the value is its leading Dv dims:
+ *   s_hj = scale * <q_h, c_j>,  state (m, l, acc) per (sequence, head,
+ *   segment) exactly as rf_attn_decode_split writes it, with v_j = c_j[:Dv].
+ * The products run on the tensor cores (S^T = C Q^T and O^T += C[:, :Dv]^T P^T,
+ * keys along the 128 TMEM lanes, heads along the columns).
+ *
+ *   q        [B, H, Dk]   bf16     query heads (already in the latent space)
+ *   c        [B, L, Dk]   bf16     latent cache, one row per key, shared by
+ *                                  the H heads of a sequence
+ *   B, H, L  sequences, query heads (a multiple of 16), keys per sequence
+ *   Dk, Dv   latent and value widths: 576 and 512 (512 latent + 64 rotary)
+ *   S        number of segments, >= 1, split as in rf_attn_decode_split
+ *            (ceil(L/S) keys each; segments past the end get the identity)
+ *   scale    score scale
+ *   seg_m    [B, H, S]      fp32 out   segment max, natural-log units
+ *   seg_l    [B, H, S]      fp32 out   sum_j exp(s_hj - seg_m)
+ *   seg_acc  [B, H, S, Dv]  fp32 out   sum_j exp(s_hj - seg_m) * c_j[:Dv]
+ * Combine with rf_state_merge(seg_m, seg_l, seg_acc, B*H, S, Dv, ...).
+ * Errors: RF_ERR_INVALID_ARG for null pointers, B, H, L <= 0, S < 1 or a
+ * non-finite scale; RF_ERR_UNSUPPORTED for (Dk, Dv) other than (576, 512),
+ * H not a multiple of 16 or B*L >= 2^31; RF_ERR_MISALIGNED unless q, c and
+ * seg_acc are 16-byte aligned; RF_ERR_TIMEOUT (through rf_device_error) if a
+ * pipeline wait inside the kernel gave up.
+ */
+rf_status rf_mla_decode_split(const void* q, const void* c, int B, int H, int L, int Dk,
+                              int Dv, int S, float scale, float* seg_m, float* seg_l,
+                              float* seg_acc, void* stream);
 
 /*
  * rf_attn_prefill -- causal prefill attention, GEMM -> online softmax -> GEMM

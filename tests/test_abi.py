@@ -179,3 +179,29 @@ def test_incremental_fp8_validation(lib):
     assert f(*args(N=256)) == 2
     assert f(*args(K=100)) == 2
     assert f(*args(x=ODD)) == 3
+
+
+def test_mla_decode_validation(lib):
+    f = lib.rf_mla_decode_split
+    args = lambda **o: [o.get("q", FAKE), o.get("c", FAKE), o.get("B", 2), o.get("H", 16),
+                        o.get("L", 300), o.get("Dk", 576), o.get("Dv", 512), o.get("S", 4),
+                        F(o.get("scale", 0.07)), FAKE, FAKE, o.get("acc", FAKE), NULL]
+    assert f(*args(q=NULL)) == 1
+    assert f(*args(c=NULL)) == 1
+    assert f(*args(B=0)) == 1
+    assert f(*args(L=0)) == 1
+    assert f(*args(S=0)) == 1
+    assert f(*args(scale=float("nan"))) == 1
+    assert f(*args(Dk=512)) == 2
+    assert f(*args(Dv=128)) == 2
+    assert f(*args(H=8)) == 2
+    assert f(*args(H=24)) == 2
+    assert f(*args(B=70000, L=32768)) == 2     # B*L rows beyond a 32-bit TMA coordinate
+    assert f(*args(q=ODD)) == 3
+    assert f(*args(acc=ODD)) == 3
+
+
+def test_merge_accepts_the_mla_value_width(lib):
+    f = lib.rf_state_merge
+    # D = 512 passes validation and fails only on the misaligned output
+    assert f(FAKE, FAKE, FAKE, 4, 8, 512, ODD, 1, NULL, NULL) == 3

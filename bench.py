@@ -193,7 +193,7 @@ def _oracle_path_samples(budget_s):
     {path: (units_done, unit, seconds, sample description)}."""
     import torch
     import synthetic_inputs as si
-    from oracle import attention, bf16, fp8, routing
+    from oracle import attention, bf16, fp8, mla, routing
 
     def timed(fn):
         n, t0 = 0, time.perf_counter()
@@ -233,6 +233,12 @@ def _oracle_path_samples(budget_s):
                            for i in rows])
     res["causal_prefill"] = (n * sum(4.0 * cfg["D"] * (i + 1) for i in rows), "FLOP", dt,
                              "16 query rows in the middle of one head (exact causal FLOPs)")
+    cfg = si.FULL["mla"]
+    qm, Cm = si.mla_inputs(1, cfg["H"], cfg["L"], cfg["Dk"], seed=si.SEEDS["mla"])
+    qm, Cm = qm.double().numpy(), Cm.double().numpy()
+    n, dt = timed(lambda: mla.mla_decode(qm, Cm, cfg["Dv"], si.mla_scale()))
+    res["mla_decode"] = (n * cfg["L"] * cfg["Dk"] * 2, "B", dt,
+                         f"one of the {cfg['B']} sequences ({cfg['H']} heads, the whole latent cache)")
     return res
 
 
@@ -490,6 +496,58 @@ def path_prefill(torch, rf, peaks):
             "roofline": roofline("tensor", tf, peaks["bf16_tflops"], "TFLOP/s", ncu_traffic("prefill"))}
 
 
+def path_mla(torch, rf, peaks):
+    """Multi-latent attention decode: B=64 sequences x 16 query heads reading
+    one shared latent cache each (L=32768 rows of 576 bf16), split into S
+    segments and merged.  The 2.4 GB cache is larger than L2."""
+    import synthetic_inputs as si
+    cfg = si.FULL["mla"]
+    B, H, L, Dk, Dv = cfg["B"], cfg["H"], cfg["L"], cfg["Dk"], cfg["Dv"]
+    q, C = si.mla_inputs(B, H, L, Dk, seed=si.SEEDS["mla"], device="cuda")
+    scale = si.mla_scale()
+    cache_bytes = B * L * Dk * 2
+    flops = 2.0 * B * H * L * (Dk + Dv)
+    res = {"workload": f"MLA decode B={B} H={H} L={L} latent {Dk} (value {Dv}) bf16, fp32 "
+                       f"accumulate, bf16 out; latent cache {cache_bytes / 1e9:.2f} GB > L2",
+           "unit": "GB/s"}
+    sweep = {}
+    for S in (8, 16, 32, 64):
+        sm = torch.empty(B, H, S, device="cuda")
+        sl = torch.empty(B, H, S, device="cuda")
+        sa = torch.empty(B, H, S, Dv, device="cuda")
+        out = torch.empty(B * H, Dv, device="cuda", dtype=torch.bfloat16)
+        lse = torch.empty(B * H, device="cuda")
+        split = lambda: rf.rf_mla_decode_split(q, C, S, scale, sm, sl, sa)
+        merge = lambda: rf.rf_state_merge(sm.view(B * H, S), sl.view(B * H, S),
+                                          sa.view(B * H, S, Dv), out, lse)
+
+        def both():
+            split()
+            merge()
+        ms = time_graph(torch, [both] * 3, 5)
+        ms_split = time_graph(torch, [split] * 3, 5)
+        state_bytes = B * H * S * (Dv + 2) * 4
+        alg = cache_bytes + q.numel() * 2 + state_bytes
+        sweep[f"S{S}"] = {"ms": round(ms, 4), "GB/s": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
+                          "split_ms": round(ms_split, 4),
+                          "split_frac_hbm": round(alg / (ms_split * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+        del sm, sl, sa, out, lse
+    best = min(sweep, key=lambda k: sweep[k]["ms"])
+    S = int(best[1:])
+    b = sweep[best]
+    alg = cache_bytes + q.numel() * 2 + B * H * S * (Dv + 2) * 4
+    res.update({"segments": S, "value": b["GB/s"], "ms_per_call": b["ms"],
+                "TFLOP/s": b["TFLOP/s"],
+                "tensor_frac": round(b["TFLOP/s"] / peaks["bf16_tflops"], 4),
+                "roofline": roofline("hbm", alg / (b["split_ms"] * 1e-3) / 1e9, peaks["hbm_gbs"],
+                                     "GB/s", ncu_traffic("mla_decode")),
+                "roofline_kernel": {"name": "mla_decode_kernel", "avg_ms": b["split_ms"],
+                                    "alg_bytes_per_launch": alg},
+                "segments_sweep": sweep})
+    return res
+
+
 def path_row_cascades(torch, rf, peaks):
     """Single-row cascades at every fusion level: softmax rows of 1K-8K
     (256 MB in, 256 MB out), variance of [16384 x 4096], moment of inertia of
@@ -573,6 +631,7 @@ def run_rf(args):
                "quant": lambda: path_quant(torch, rf, peaks),
                "gemm": lambda: path_gemm(torch, rf, peaks),
                "prefill": lambda: path_prefill(torch, rf, peaks),
+               "mla": lambda: path_mla(torch, rf, peaks),
                "rows": lambda: path_row_cascades(torch, rf, peaks),
                "ablation": lambda: decode_ablation(
                    torch, rf, peaks, *si.decode_inputs(1024, 32768, 128, torch.bfloat16, seed=2,
@@ -671,6 +730,7 @@ def run_rf(args):
                          ("absmax_quant_e4m3", lambda: path_quant(torch, rf, peaks)),
                          ("fp8_gemm", lambda: path_gemm(torch, rf, peaks)),
                          ("causal_prefill", lambda: path_prefill(torch, rf, peaks)),
+                         ("mla_decode", lambda: path_mla(torch, rf, peaks)),
                          ("row_cascades", lambda: path_row_cascades(torch, rf, peaks))):
             try:
                 paths[name] = fn()
@@ -754,7 +814,7 @@ def main():
     ap.add_argument("--rows", type=int, default=0,
                     help="decode rows instead of B*H=1024 (small cases for ncu captures)")
     ap.add_argument("--decode-only", action="store_true", help="skip the other cascades")
-    ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm",
+    ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm", "mla",
                                        "prefill", "rows", "ablation"],
                     help="time one other cascade alone")
     ap.add_argument("--no-e2e", action="store_true")

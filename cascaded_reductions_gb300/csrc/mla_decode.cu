@@ -23,6 +23,9 @@
 // rope slot.  Five pair slots leave one for the next tile while the current
 // one is in use.
 //
+// Each pair slot is released as soon as the O^T MMAs that read it complete,
+// so the next tile's loads start during the current tile's P V product.
+//
 // Warps: 0 TMA, 1 MMA (and TMEM owner), 2-5 softmax (one thread per key of
 // the tile, i.e. per TMEM lane).  Persistent CTAs take contiguous ranges of
 // (sequence, head group, segment) units, so Q is reloaded only when the
@@ -308,8 +311,8 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                              tc::sdesc_sw128(p_addr + (ks >> 2) * HG * 128 + (ks & 3) * 32, 16,
                                              1024),
                              idesc_o, (t > 0 || ks > 0) ? 1u : 0u);
+            tc::mma_commit(&sh->pair_empty[slots[c]]);     // this pair is free once read
           }
-          for (int p = 0; p < 4; ++p) tc::mma_commit(&sh->pair_empty[slots[p]]);
           tc::mma_commit(&sh->o_done);
           np += 4;
         }

@@ -5,6 +5,10 @@
 // exp-sum denominator and the k largest entries all come from a single pass
 // over the logits held in registers.
 //
+// Two kernels.  For E <= 128 (with k <= G), softmax_topk_merge_kernel: each
+// lane keeps its best two logits and the group merges lane heads round by
+// round (below).  Otherwise softmax_topk_kernel:
+//
 // Layout: a group of G lanes (G = 8, 16 or 32) owns TPG tokens, one after the
 // other; lane g of the group holds NV logits of each token, loaded W at a
 // time (W = 4, 2 or 1 consecutive floats, coalesced across the group).  With
@@ -40,6 +44,7 @@ namespace rf {
 namespace {
 
 constexpr uint32_t FULL = 0xffffffffu;
+
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x + 0.0f);     // -0 -> +0
@@ -250,6 +255,177 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k_rt, in
   }
 }
 
+// Per-lane top-2, then a k-way merge over the group's lanes.
+//
+// Each lane scans its NV slots once (slot order is expert order, and a strict
+// comparison keeps the lower expert first among equal values) and keeps its
+// best two as (order key, slot).  Round r of the merge: every lane offers its
+// head; the group takes the largest key with one redux.sync and the lowest
+// expert among the lanes offering it with a second; the winner pops its head,
+// which becomes its second best.  A lane that wins a third time has no
+// precomputed successor, so it rescans its untaken slots (a branch only that
+// lane takes).  Every round therefore sees each lane's true best untaken
+// value, and the result is the exact top-k with ties by lower expert index,
+// for any k <= G.
+// the group's NV logits of one token (-inf for padding slots and past T)
+template <int G, int NV, int W>
+__device__ __forceinline__ void load_token(const float* __restrict__ logits, int T, int E, int token,
+                                           int gl, float (&x)[NV]) {
+  const bool live = token < T;
+  const float* row = logits + (size_t)(live ? token : 0) * E;
+#pragma unroll
+  for (int c = 0; c < NV / W; ++c) {
+    const int e0 = c * G * W + gl * W;
+    const bool in = live && e0 < E;
+    if (W == 4) {
+      const float4 f = in ? __ldcs(reinterpret_cast<const float4*>(row + e0))
+                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      x[4 * c + 0] = f.x;
+      x[4 * c + 1] = f.y;
+      x[4 * c + 2] = f.z;
+      x[4 * c + 3] = f.w;
+    } else {
+      x[c] = in ? __ldcs(row + e0) : -INFINITY;
+    }
+  }
+}
+
+template <int G, int NV, int W, int KT>
+__device__ __forceinline__ void merge_select(const float (&x)[NV], int token, int T, int k,
+                                             int renorm, int gl, uint32_t gmask,
+                                             int32_t* __restrict__ idx_out,
+                                             float* __restrict__ w_out) {
+  auto expert = [&](int i) -> int { return (i / W) * G * W + gl * W + (i % W); };
+  // Padding slots (expert >= E) hold -inf and come after every real slot of
+  // the lane in slot order, and after every real expert in index order, so
+  // they are never chosen while k <= E and add 0 to the softmax sum.
+  {
+    // the lane's best two slots, compared as floats (-0 == +0, as the keys)
+    float v1 = x[0], v2 = -INFINITY;
+    int s1 = 0, s2 = -1;
+    if (NV > 1) {
+      const bool sw = x[1] > x[0];
+      v1 = sw ? x[1] : x[0];
+      s1 = sw ? 1 : 0;
+      v2 = sw ? x[0] : x[1];
+      s2 = sw ? 0 : 1;
+    }
+#pragma unroll
+    for (int i = 2; i < NV; ++i) {
+      const bool c1 = x[i] > v1, c2 = x[i] > v2;
+      v2 = c1 ? v1 : (c2 ? x[i] : v2);
+      s2 = c1 ? s1 : (c2 ? i : s2);
+      v1 = c1 ? x[i] : v1;
+      s1 = c1 ? i : s1;
+    }
+    uint32_t k1 = order_key(v1), k2 = s2 >= 0 ? order_key(v2) : 0u;
+    int e1 = expert(s1), e2 = s2 >= 0 ? expert(s2) : 0x7fffffff;
+    uint32_t taken = 0u;
+    bool have_next = true;
+    uint32_t mykey = 0u;
+    int myidx = 0;
+#pragma unroll
+    for (int r = 0; r < (KT > 0 ? KT : 32); ++r) {
+      if (KT == 0 && r >= k) break;
+      const uint32_t g = __reduce_max_sync(gmask, k1);
+      const int gi = (int)__reduce_min_sync(gmask, k1 == g ? (uint32_t)e1 : 0x7fffffffu);
+      if (gl == r) {
+        mykey = g;
+        myidx = gi;
+      }
+      if (k1 == g && e1 == gi) {
+        taken |= 1u << s1;
+        if (have_next) {
+          k1 = k2;
+          e1 = e2;
+          s1 = s2;
+          have_next = false;
+        } else {
+          // third pop of this lane: its best untaken slot
+          int b = -1;
+          float bv = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < NV; ++i)
+            if (!((taken >> i) & 1u) && (b < 0 || x[i] > bv)) {
+              b = i;
+              bv = x[i];
+            }
+          k1 = b >= 0 ? order_key(bv) : 0u;
+          e1 = b >= 0 ? expert(b) : 0x7fffffff;
+          s1 = b;
+        }
+      }
+    }
+    const float m = key_value(__shfl_sync(FULL, mykey, 0, G));
+    const float w = gl < k ? __expf(key_value(mykey) - m) : 0.f;
+    float denom;
+    if (renorm) {
+      denom = gsum<G>(w, k);
+    } else {
+      float l = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) l += __expf(x[i] - m);
+      denom = gsum<G>(l, G);
+    }
+    if (token < T && gl < k) {
+      idx_out[(size_t)token * k + gl] = myidx;
+      w_out[(size_t)token * k + gl] = __fdividef(w, denom);
+    }
+  }
+}
+
+// Grid-stride over tokens: each group loads the logits of its next token into
+// a second register buffer before it selects from the current one, so the
+// loads of one token are in flight under the selection work of the previous.
+// The loop bound is uniform across the warp (groups past T select from -inf
+// and store nothing), so full-warp shuffles stay legal.
+template <int G, int NV, int W, int KT>
+__global__ void __launch_bounds__(256)
+softmax_topk_merge_kernel(const float* __restrict__ logits, int T, int E, int k_rt, int renorm,
+                          int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+  static_assert(NV % W == 0 && NV <= 32 && 32 % G == 0, "layout");
+  constexpr int GPW = 32 / G;
+  const int k = KT > 0 ? KT : k_rt;
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const uint32_t gmask = G == 32 ? FULL : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const int warp_global = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int stride = (int)((gridDim.x * blockDim.x) >> 5) * GPW;
+  int base = warp_global * GPW;                      // the warp's first token, uniform
+  const int grp = lane / G;
+  float xa[NV], xb[NV];
+  load_token<G, NV, W>(logits, T, E, base + grp, gl, xa);
+  while (base < T) {
+    load_token<G, NV, W>(logits, T, E, base + stride + grp, gl, xb);
+    merge_select<G, NV, W, KT>(xa, base + grp, T, k, renorm, gl, gmask, idx_out, w_out);
+    base += stride;
+    if (base >= T) break;
+    load_token<G, NV, W>(logits, T, E, base + stride + grp, gl, xa);
+    merge_select<G, NV, W, KT>(xb, base + grp, T, k, renorm, gl, gmask, idx_out, w_out);
+    base += stride;
+  }
+}
+
+constexpr int kMergeBlocksPerSm = 8;     // measured best of 2, 4, 8, 16 at [65536 x 64]
+
+template <int G, int NV, int W>
+void launch_merge(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
+                  cudaStream_t st) {
+  constexpr int tokens_per_block = 256 / G;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long need = (T + tokens_per_block - 1) / tokens_per_block;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * kMergeBlocksPerSm;
+  const unsigned grid = (unsigned)(need < cap ? need : cap);
+  if (k == 8)
+    softmax_topk_merge_kernel<G, NV, W, 8><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
+  else if (k == 2)
+    softmax_topk_merge_kernel<G, NV, W, 2><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
+  else
+    softmax_topk_merge_kernel<G, NV, W, 0><<<grid, 256, 0, st>>>(logits, T, E, k, renorm, idx, w);
+}
+
 template <int G, int NV, int W, int TPG, bool THRESH>
 void launch_one(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w,
                 cudaStream_t st) {
@@ -269,12 +445,15 @@ rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int reno
                               int32_t* idx, float* w, cudaStream_t st) {
   const bool v4 = E % 4 == 0;
   // lanes r < k of a group keep round r's winner, so G >= k
-  if (E <= 64 && k <= 8) {
-    if (v4) launch_one<8, 8, 4, 2, false>(logits, T, E, k, renormalize, idx, w, st);
-    else launch_one<8, 8, 1, 2, false>(logits, T, E, k, renormalize, idx, w, st);
+  if (E <= 64 && k <= 4) {
+    if (v4) launch_merge<4, 16, 4>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_merge<4, 16, 1>(logits, T, E, k, renormalize, idx, w, st);
+  } else if (E <= 64 && k <= 8) {
+    if (v4) launch_merge<8, 8, 4>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_merge<8, 8, 1>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 128 && k <= 16) {
-    if (v4) launch_one<16, 8, 4, 1, false>(logits, T, E, k, renormalize, idx, w, st);
-    else launch_one<16, 8, 1, 1, false>(logits, T, E, k, renormalize, idx, w, st);
+    if (v4) launch_merge<16, 8, 4>(logits, T, E, k, renormalize, idx, w, st);
+    else launch_merge<16, 8, 1>(logits, T, E, k, renormalize, idx, w, st);
   } else if (E <= 128) {
     if (v4) launch_one<32, 4, 4, 2, false>(logits, T, E, k, renormalize, idx, w, st);
     else launch_one<32, 4, 1, 2, false>(logits, T, E, k, renormalize, idx, w, st);

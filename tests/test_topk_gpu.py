@@ -63,3 +63,35 @@ def test_ties_lower_index_first(rf):
 def test_single_token(rf):
     x = si.routing_logits(1, 256, seed=1)
     check(rf, x, 8, True, "T=1")
+
+
+@pytest.mark.parametrize("E,k", [(64, 1), (64, 3), (64, 4), (60, 4), (61, 2), (64, 8), (47, 6),
+                                 (128, 16), (120, 9), (256, 1), (256, 5), (200, 8), (253, 8)])
+def test_merge_shapes(rf, E, k):
+    x = si.routing_logits(301, E, seed=E * 13 + k)
+    check(rf, x, k, True, f"E={E} k={k}")
+    check(rf, x, k, False, f"E={E} k={k} no renorm")
+
+
+@pytest.mark.parametrize("E,k", [(256, 8), (64, 2), (64, 4), (128, 16)])
+def test_top_values_in_one_lane(rf, E, k):
+    # every one of the k largest logits sits in the slots of one lane, so that
+    # lane wins round after round and must rescan its untaken slots
+    T = 96
+    x = si.routing_logits(T, E, seed=5)
+    G, W = {256: 32, 64: 4 if k <= 4 else 8, 128: 16}[E], 4
+    nv = E // G
+    for t in range(T):
+        lane = t % G
+        slots = [(i // W) * G * W + lane * W + (i % W) for i in range(nv)]
+        for j, e in enumerate(slots[:k]):
+            x[t, e] = 50.0 - j if t % 2 else 50.0 - (k - 1 - j)   # both orders
+    check(rf, x, k, True, f"one-lane E={E} k={k}")
+
+
+def test_neg_inf_logits(rf):
+    x = si.routing_logits(64, 256, seed=6)
+    x[:, ::3] = -float("inf")
+    x[7, :] = -float("inf")
+    x[7, 200] = 1.0       # one finite logit: the rest are -inf ties, lower index first
+    check(rf, x, 8, True, "-inf logits")

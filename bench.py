@@ -496,7 +496,7 @@ def path_prefill(torch, rf, peaks):
             "roofline": roofline("tensor", tf, peaks["bf16_tflops"], "TFLOP/s", ncu_traffic("prefill"))}
 
 
-def path_mla(torch, rf, peaks):
+def path_mla(torch, rf, peaks, only_segments=0):
     """Multi-latent attention decode: B=64 sequences x 16 query heads reading
     one shared latent cache each (L=32768 rows of 576 bf16), split into S
     segments and merged.  The 2.4 GB cache is larger than L2."""
@@ -511,7 +511,7 @@ def path_mla(torch, rf, peaks):
                        f"accumulate, bf16 out; latent cache {cache_bytes / 1e9:.2f} GB > L2",
            "unit": "GB/s"}
     sweep = {}
-    for S in (8, 16, 32, 64):
+    for S in ((only_segments,) if only_segments else (8, 16, 32, 64)):
         sm = torch.empty(B, H, S, device="cuda")
         sl = torch.empty(B, H, S, device="cuda")
         sa = torch.empty(B, H, S, Dv, device="cuda")
@@ -631,7 +631,7 @@ def run_rf(args):
                "quant": lambda: path_quant(torch, rf, peaks),
                "gemm": lambda: path_gemm(torch, rf, peaks),
                "prefill": lambda: path_prefill(torch, rf, peaks),
-               "mla": lambda: path_mla(torch, rf, peaks),
+               "mla": lambda: path_mla(torch, rf, peaks, args.mla_segments),
                "rows": lambda: path_row_cascades(torch, rf, peaks),
                "ablation": lambda: decode_ablation(
                    torch, rf, peaks, *si.decode_inputs(1024, 32768, 128, torch.bfloat16, seed=2,
@@ -817,6 +817,8 @@ def main():
     ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm", "mla",
                                        "prefill", "rows", "ablation"],
                     help="time one other cascade alone")
+    ap.add_argument("--mla-segments", type=int, default=0,
+                    help="with --only mla: time this segment count alone (profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work")

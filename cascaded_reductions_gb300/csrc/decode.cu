@@ -163,16 +163,22 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
   }
 }
 
-// One warp per row.  Lane j owns 4 consecutive elements of every 128-wide
-// block of D (D = 128, 512), or lanes 0..15 own them (D = 64); the segment
-// weights exp(m_s - M) are computed by every lane from the (cached) seg_m row.
+// One warp per (row, 128-wide block of D) -- D/128 warps per row for D >= 128,
+// one for D = 64.  Lane j owns 4 consecutive elements of the block (lanes
+// 0..15 for D = 64); every warp of a row recomputes the row's segment weights
+// exp(m_s - M) from seg_m (S values, cached), and the first writes lse.
 template <int D, bool BF16_OUT>
 __global__ void __launch_bounds__(256)
 state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ seg_l,
                    const float* __restrict__ seg_acc, int R, int S, void* __restrict__ out,
                    float* __restrict__ lse) {
+  constexpr int PARTS = D >= 128 ? D / 128 : 1;
+  constexpr int V4 = D / 4;                     // float4s per state
+  constexpr int LANES = V4 < 32 ? V4 : 32;      // float4s of this warp's block
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long long wid = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int row = (int)(wid / PARTS);
+  const int part = (int)(wid % PARTS);
   if (row >= R) return;
   const float* mr = seg_m + (size_t)row * S;
   const float* lr = seg_l + (size_t)row * S;
@@ -186,41 +192,31 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
   for (int s = lane; s < S; s += 32) Lsum = fmaf(expf(mr[s] - ref), lr[s], Lsum);
   Lsum = group_sum<32>(Lsum);
 
-  constexpr int V4 = D / 4;                     // float4s per state
-  constexpr int NB = V4 < 32 ? 1 : V4 / 32;     // float4s per lane
-  if (lane < V4) {
-    float4 A[NB];
-#pragma unroll
-    for (int i = 0; i < NB; ++i) A[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* ar = reinterpret_cast<const float4*>(seg_acc + (size_t)row * S * D) + lane;
+  if (lane < LANES) {
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* ar =
+        reinterpret_cast<const float4*>(seg_acc + (size_t)row * S * D) + part * 32 + lane;
     for (int s = 0; s < S; ++s) {
       const float f = expf(mr[s] - ref);
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        const float4 x = ar[(size_t)s * V4 + 32 * i];
-        A[i].x = fmaf(f, x.x, A[i].x);
-        A[i].y = fmaf(f, x.y, A[i].y);
-        A[i].z = fmaf(f, x.z, A[i].z);
-        A[i].w = fmaf(f, x.w, A[i].w);
-      }
+      const float4 x = ar[(size_t)s * V4];
+      A.x = fmaf(f, x.x, A.x);
+      A.y = fmaf(f, x.y, A.y);
+      A.z = fmaf(f, x.z, A.z);
+      A.w = fmaf(f, x.w, A.w);
     }
     const float inv = 1.f / Lsum;
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      float4 a = A[i];
-      a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
-      const size_t o = (size_t)row * V4 + lane + 32 * i;
-      if (BF16_OUT) {
-        uint2 p;
-        p.x = pack_bf16x2(a.x, a.y);
-        p.y = pack_bf16x2(a.z, a.w);
-        reinterpret_cast<uint2*>(out)[o] = p;
-      } else {
-        reinterpret_cast<float4*>(out)[o] = a;
-      }
+    A.x *= inv; A.y *= inv; A.z *= inv; A.w *= inv;
+    const size_t o = (size_t)row * V4 + part * 32 + lane;
+    if (BF16_OUT) {
+      uint2 p;
+      p.x = pack_bf16x2(A.x, A.y);
+      p.y = pack_bf16x2(A.z, A.w);
+      reinterpret_cast<uint2*>(out)[o] = p;
+    } else {
+      reinterpret_cast<float4*>(out)[o] = A;
     }
   }
-  if (lse != nullptr && lane == 0) lse[row] = M + logf(Lsum);
+  if (lse != nullptr && lane == 0 && part == 0) lse[row] = M + logf(Lsum);
 }
 
 }  // namespace
@@ -249,7 +245,8 @@ rf_status launch_decode_split(const void* q, const void* k, const void* v, int R
 
 rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc, int R,
                              int S, int D, void* out, int out_dtype, float* lse, cudaStream_t st) {
-  const unsigned grid = (unsigned)((R + 7) / 8);
+  const long long warps = (long long)R * (D >= 128 ? D / 128 : 1);
+  const unsigned grid = (unsigned)((warps + 7) / 8);
   const bool bf = out_dtype == RF_BF16;
   if (D == 128) {
     if (bf) state_merge_kernel<128, true><<<grid, 256, 0, st>>>(seg_m, seg_l, seg_acc, R, S, out, lse);

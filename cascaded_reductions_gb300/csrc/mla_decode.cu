@@ -26,15 +26,16 @@
 // Each pair slot is released as soon as the O^T MMAs that read it complete,
 // so the next tile's loads start during the current tile's P V product.
 //
-// Warps: 0 TMA, 1 MMA (and TMEM owner), 2-5 softmax (one thread per key of
-// the tile, i.e. per TMEM lane).  Persistent CTAs take contiguous ranges of
+// Warps: 0 TMA, 1 MMA (and TMEM owner), 2-9 softmax: two warps per TMEM lane
+// quarter, each thread one key of the tile (one TMEM lane) and half of the
+// heads, so each SM sub-partition interleaves two short softmax chains.  Persistent CTAs take contiguous ranges of
 // (sequence, head group, segment) units, so Q is reloaded only when the
 // sequence or head group changes.
 //
 // Per tile: S^T MMAs (rope chunk first, then the eight value chunks); each
-// softmax thread loads its key's HG scores, the tile max per head is reduced
-// over the warp (redux on order-preserving integer keys) and over the four
-// warps (shared memory + an mbarrier), the reference max moves lazily (only
+// softmax thread loads its key's scores for its HG/2 heads, the tile max per
+// head is reduced over the warp (redux on order-preserving integer keys) and
+// over the four lane quarters (shared memory + an mbarrier per head half), the reference max moves lazily (only
 // when a head's tile max exceeds it by more than 8 in log2 units, rescaling
 // that head's column of O^T in TMEM and its partial l), P^T is written to
 // shared memory as bf16 in the 128-byte-swizzled K-major layout, and the MMA
@@ -57,7 +58,7 @@ constexpr int BK = 128;                    // keys per tile
 constexpr int CHUNK = BK * 128;            // one 64-dim box of a tile: 16 KiB
 constexpr int PAIR = 2 * CHUNK;            // 128 value dims: 32 KiB
 constexpr int NPAIR = 5;                   // pair slots (4 per tile + 1 ahead)
-constexpr int THREADS = 6 * 32;
+constexpr int THREADS = 10 * 32;          // TMA, MMA, 8 softmax warps
 constexpr int TMA_WARP = 0, MMA_WARP = 1;
 constexpr int TMEM_COLS = 256;
 constexpr uint32_t S_COL = 0;              // S^T: HG columns
@@ -69,7 +70,7 @@ struct MlaShared {
   uint64_t rope_full, rope_empty;
   uint64_t pair_full[NPAIR], pair_empty[NPAIR];
   uint64_t s_full, p_full, o_done;
-  uint64_t red_ready[2], l_ready, drain;
+  uint64_t red_ready[2][2], l_ready, drain;     // red_ready[tile parity][head half]
   float red[2][4][32];                     // [tile parity][warp][head] tile maxima
   float lred[4][32];                       // [warp][head] partial l
   uint32_t tmem_base;
@@ -127,6 +128,10 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_m
 template <int HG>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[HG]);
 template <>
+__device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t (&r)[8]) {
+  tc::tmem_ld_32x32b_x8(taddr, r);
+}
+template <>
 __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&r)[16]) {
   tc::tmem_ld_32x32b_x16(taddr, r);
 }
@@ -134,14 +139,18 @@ template <>
 __device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, uint32_t (&r)[32]) {
   tc::tmem_ld_32x32b_x32(taddr, r);
 }
-template <int HG>
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[HG]) {
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 8) {
+    tc::tmem_st_32x32b_x8(taddr, r);
+  } else {
 #pragma unroll
-  for (int h0 = 0; h0 < HG; h0 += 16) {
-    uint32_t w[16];
+    for (int h0 = 0; h0 < N; h0 += 16) {
+      uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = r[h0 + i];
-    tc::tmem_st_32x32b_x16(taddr + (uint32_t)h0, w);
+      for (int i = 0; i < 16; ++i) w[i] = r[h0 + i];
+      tc::tmem_st_32x32b_x16(taddr + (uint32_t)h0, w);
+    }
   }
 }
 
@@ -177,11 +186,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       tc::mbar_init(&sh->pair_empty[i], 1);
     }
     tc::mbar_init(&sh->s_full, 1);
-    tc::mbar_init(&sh->p_full, 4);
+    tc::mbar_init(&sh->p_full, 8);
     tc::mbar_init(&sh->o_done, 1);
-    tc::mbar_init(&sh->red_ready[0], 4);
-    tc::mbar_init(&sh->red_ready[1], 4);
-    tc::mbar_init(&sh->l_ready, 4);
+    for (int i = 0; i < 2; ++i)
+      for (int j = 0; j < 2; ++j) tc::mbar_init(&sh->red_ready[i][j], 4);
+    tc::mbar_init(&sh->l_ready, 8);
     tc::mbar_init(&sh->drain, 1);
     sh->abort = 0;
     tc::fence_barrier_init();
@@ -323,10 +332,13 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     }
   } else {
     // -------------------------------------------------------- softmax ----
+    // warps 2..9: two per TMEM lane quarter, each owning HW = HG/2 heads
+    constexpr int HW = HG / 2;
     const int quarter = warp & 3;                   // TMEM lane quarter of this warp
+    const int hh = (warp - 2) >> 2;                 // which half of the heads
+    const int hb = hh * HW;                         // first head of this warp
     const int kt = quarter * 32 + lane;             // key of the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int wsm = warp - 2;                       // 0..3 among the softmax warps
     uint32_t nt_all = 0, nunits = 0;
     bool ok = true;
     for (long long u = u0; u < u1 && ok; ++u) {
@@ -334,17 +346,17 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       const size_t st0 = ((size_t)x.b * H + (size_t)x.g * HG) * S + x.s;   // state of head 0
       if (x.nt == 0) {
         // empty segment: the identity state
-        for (int i = threadIdx.x - 64; i < HG * DV; i += 128)
+        for (int i = threadIdx.x - 64; i < HG * DV; i += THREADS - 64)
           seg_acc[(st0 + (size_t)(i / DV) * S) * DV + (i % DV)] = 0.f;
-        if (kt < HG) {
-          seg_m[st0 + (size_t)kt * S] = -INFINITY;
-          seg_l[st0 + (size_t)kt * S] = 0.f;
+        if (quarter == 0 && lane < HW) {
+          seg_m[st0 + (size_t)(hb + lane) * S] = -INFINITY;
+          seg_l[st0 + (size_t)(hb + lane) * S] = 0.f;
         }
         continue;
       }
-      float mref[HG], mtrue[HG], lp[HG];
+      float mref[HW], mtrue[HW], lp[HW];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int h = 0; h < HW; ++h) {
         mref[h] = -INFINITY;
         mtrue[h] = -INFINITY;
         lp[h] = 0.f;
@@ -352,31 +364,31 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       for (int t = 0; t < x.nt; ++t, ++nt_all) {
         if (!(ok = tc::mbar_wait(&sh->s_full, nt_all & 1u, abort))) break;
         tc::fence_after_sync();
-        float sv[HG];
+        float sv[HW];
         {
-          uint32_t r[HG];
-          tmem_ld_cols<HG>(lane_base + S_COL, r);
+          uint32_t r[HW];
+          tmem_ld_cols<HW>(lane_base + S_COL + (uint32_t)hb, r);
           tc::tmem_ld_wait();
           const bool valid = x.a + t * BK + kt < x.e;
 #pragma unroll
-          for (int h = 0; h < HG; ++h) sv[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
+          for (int h = 0; h < HW; ++h) sv[h] = valid ? __uint_as_float(r[h]) * scale_log2 : -INFINITY;
         }
-        // tile max per head: over the warp, then over the four warps
+        // tile max per head: over the warp, then over the four lane quarters
         const int par = (int)(nt_all & 1u);
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
+        for (int h = 0; h < HW; ++h) {
           const uint32_t k = __reduce_max_sync(0xffffffffu, order_key(sv[h]));
-          if (lane == h) sh->red[par][wsm][h] = order_key_inv(k);
+          if (lane == h) sh->red[par][quarter][hb + h] = order_key_inv(k);
         }
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&sh->red_ready[par]);
-        if (!(ok = tc::mbar_wait(&sh->red_ready[par], (nt_all >> 1) & 1u, abort))) break;
-        float alpha[HG];
+        if (lane == 0) tc::mbar_arrive(&sh->red_ready[par][hh]);
+        if (!(ok = tc::mbar_wait(&sh->red_ready[par][hh], (nt_all >> 1) & 1u, abort))) break;
+        float alpha[HW];
         bool any_move = false;
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float tm = fmaxf(fmaxf(sh->red[par][0][h], sh->red[par][1][h]),
-                                 fmaxf(sh->red[par][2][h], sh->red[par][3][h]));
+        for (int h = 0; h < HW; ++h) {
+          const float tm = fmaxf(fmaxf(sh->red[par][0][hb + h], sh->red[par][1][hb + h]),
+                                 fmaxf(sh->red[par][2][hb + h], sh->red[par][3][hb + h]));
           mtrue[h] = fmaxf(mtrue[h], tm);
           const bool move = tm > mref[h] + RESCALE_THRESHOLD;
           const float mn = move ? tm : mref[h];
@@ -384,21 +396,21 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           any_move |= move;
           mref[h] = mn;
         }
-        // P^T V^T product of the previous tile must be done before P^T is
-        // overwritten and before O^T is rescaled
+        // the previous tile's O^T MMAs must be done before P^T is overwritten
+        // and before O^T is rescaled
         if (t > 0) {
           if (!(ok = tc::mbar_wait(&sh->o_done, (nt_all - 1) & 1u, abort))) break;
           tc::fence_after_sync();
           if (any_move) {
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
-              const uint32_t oc = lane_base + O_COL + (uint32_t)(c * HG);
-              uint32_t r[HG];
-              tmem_ld_cols<HG>(oc, r);
+              const uint32_t oc = lane_base + O_COL + (uint32_t)(c * HG + hb);
+              uint32_t r[HW];
+              tmem_ld_cols<HW>(oc, r);
               tc::tmem_ld_wait();
 #pragma unroll
-              for (int h = 0; h < HG; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * alpha[h]);
-              tmem_st_cols<HG>(oc, r);
+              for (int h = 0; h < HW; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * alpha[h]);
+              tmem_st_cols<HW>(oc, r);
             }
             tc::tmem_st_wait();
           }
@@ -408,10 +420,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           uint8_t* chunk = sP + (kt >> 6) * HG * 128;
           const int gran = (kt & 63) >> 3;
 #pragma unroll
-          for (int h = 0; h < HG; ++h) {
+          for (int j = 0; j < HW; ++j) {
+            const int h = hb + j;
             // l sums the same bf16-rounded weights the MMA multiplies V by
-            const __nv_bfloat16 pb = __float2bfloat16_rn(ex2(sv[h] - mref[h]));
-            lp[h] = fmaf(lp[h], alpha[h], __bfloat162float(pb));
+            const __nv_bfloat16 pb = __float2bfloat16_rn(ex2(sv[j] - mref[j]));
+            lp[j] = fmaf(lp[j], alpha[j], __bfloat162float(pb));
             const uint32_t off = (uint32_t)(h * 128 + ((gran ^ (h & 7)) << 4) + ((kt & 7) << 1));
             *reinterpret_cast<__nv_bfloat16*>(chunk + off) = pb;
           }
@@ -425,37 +438,38 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       // ---- end of the unit: states relative to the true segment max
       if (!(ok = tc::mbar_wait(&sh->o_done, (nt_all - 1) & 1u, abort))) break;
       tc::fence_after_sync();
-      float f[HG];
+      float f[HW];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
+      for (int h = 0; h < HW; ++h) {
         f[h] = ex2(mref[h] - mtrue[h]);
         const float w = group_sum<32>(lp[h]);
-        if (lane == h) sh->lred[wsm][h] = w;
+        if (lane == h) sh->lred[quarter][hb + h] = w;
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->l_ready);
       if (!(ok = tc::mbar_wait(&sh->l_ready, nunits & 1u, abort))) break;
       ++nunits;
-      if (kt < HG) {
+      if (quarter == 0 && lane < HW) {
         float fk = 0.f, mk = 0.f;
 #pragma unroll
-        for (int h = 0; h < HG; ++h)
-          if (h == kt) {
+        for (int h = 0; h < HW; ++h)
+          if (h == lane) {
             fk = f[h];
             mk = mtrue[h];
           }
-        const float lt = (sh->lred[0][kt] + sh->lred[1][kt]) + (sh->lred[2][kt] + sh->lred[3][kt]);
-        seg_l[st0 + (size_t)kt * S] = lt * fk;
-        seg_m[st0 + (size_t)kt * S] = mk * kLn2;
+        const int hd = hb + lane;
+        const float lt = (sh->lred[0][hd] + sh->lred[1][hd]) + (sh->lred[2][hd] + sh->lred[3][hd]);
+        seg_l[st0 + (size_t)hd * S] = lt * fk;
+        seg_m[st0 + (size_t)hd * S] = mk * kLn2;
       }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
-        uint32_t r[HG];
-        tmem_ld_cols<HG>(lane_base + O_COL + (uint32_t)(c * HG), r);
+        uint32_t r[HW];
+        tmem_ld_cols<HW>(lane_base + O_COL + (uint32_t)(c * HG + hb), r);
         tc::tmem_ld_wait();
-        float* dst = seg_acc + st0 * DV + c * BK + kt;
+        float* dst = seg_acc + (st0 + (size_t)hb * S) * DV + c * BK + kt;
 #pragma unroll
-        for (int h = 0; h < HG; ++h) dst[(size_t)h * S * DV] = __uint_as_float(r[h]) * f[h];
+        for (int h = 0; h < HW; ++h) dst[(size_t)h * S * DV] = __uint_as_float(r[h]) * f[h];
       }
       tc::fence_before_sync();
     }

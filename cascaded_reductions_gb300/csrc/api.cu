@@ -108,7 +108,7 @@ rf_status rf_absmax_quant_e4m3(const void* x, int M, int K, uint8_t* xq, float* 
 
 static rf_status check_gemm_shape(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0) return RF_ERR_INVALID_ARG;
-  if (M % 128 != 0 || N % 256 != 0 || K % 128 != 0 || K > 65536) return RF_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || K > 65536) return RF_ERR_UNSUPPORTED;
   return RF_OK;
 }
 
@@ -117,7 +117,8 @@ rf_status rf_fp8_gemm_scaled(const uint8_t* xq, const float* sx, const uint8_t* 
   if (!xq || !sx || !wq || !sw || !y) return RF_ERR_INVALID_ARG;
   rf_status s = check_gemm_shape(M, N, K);
   if (s != RF_OK) return s;
-  if (!rf::aligned16(xq) || !rf::aligned16(wq) || !rf::aligned16(y)) return RF_ERR_MISALIGNED;
+  if (!rf::aligned16(xq) || !rf::aligned16(wq) || !rf::aligned16(y) || !rf::aligned16(sw))
+    return RF_ERR_MISALIGNED;
   return rf::launch_fp8_gemm(xq, sx, wq, sw, M, N, K, y, as_stream(stream));
 }
 
@@ -126,7 +127,8 @@ rf_status rf_absmax_quant_fp8_gemm(const void* x, int M, int K, const uint8_t* w
   if (!x || !wq || !sw || !xq || !sx || !y) return RF_ERR_INVALID_ARG;
   rf_status s = check_gemm_shape(M, N, K);
   if (s != RF_OK) return s;
-  if (!rf::aligned16(x) || !rf::aligned16(wq) || !rf::aligned16(xq) || !rf::aligned16(y))
+  if (!rf::aligned16(x) || !rf::aligned16(wq) || !rf::aligned16(xq) || !rf::aligned16(y) ||
+      !rf::aligned16(sw))
     return RF_ERR_MISALIGNED;
   s = rf::launch_absmax_quant(x, M, K, xq, sx, as_stream(stream));
   if (s != RF_OK) return s;

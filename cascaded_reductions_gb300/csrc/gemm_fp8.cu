@@ -58,9 +58,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   Shared* sh = reinterpret_cast<Shared*>(smem + (size_t)STAGES * STAGE_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int tiles_n = N / BN;
-  const int num_tiles = (M / BM) * tiles_n;
-  const int num_k = K / BK;
+  // ragged edges: the tensor maps zero-fill rows past M / N and columns past
+  // K (an e4m3 zero adds nothing), the epilogue masks what it stores
+  const int tiles_n = (N + BN - 1) / BN;
+  const int num_tiles = ((M + BM - 1) / BM) * tiles_n;
+  const int num_k = (K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -156,27 +158,42 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       tc::fence_after_sync();
       const int tm = tile / tiles_n, tn = tile - (tile / tiles_n) * tiles_n;
       const int row = tm * BM + r;
-      const float srow = sx[row];
-      __nv_bfloat16* yrow = y + (size_t)row * N + (size_t)tn * BN;
-      const float4* swv = reinterpret_cast<const float4*>(sw + (size_t)tn * BN);
+      const bool row_in = row < M;
+      const float srow = row_in ? sx[row] : 0.f;
+      __nv_bfloat16* yrow = y + (size_t)(row_in ? row : 0) * N;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = tn * BN + c * 32;
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);
+        tc::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);   // whole warp, every row
         tc::tmem_ld_wait();
-        uint32_t p[16];
+        if (!row_in || col0 >= N) continue;
+        if (col0 + 32 <= N && (N & 7) == 0) {
+          // whole 32-column chunk, 16-byte aligned row: vector loads and stores
+          const float4* swv = reinterpret_cast<const float4*>(sw + col0);
+          uint32_t p[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 s4 = __ldg(swv + c * 8 + j);
-          p[2 * j] = pack_bf16x2(__uint_as_float(v[4 * j]) * srow * s4.x,
-                                 __uint_as_float(v[4 * j + 1]) * srow * s4.y);
-          p[2 * j + 1] = pack_bf16x2(__uint_as_float(v[4 * j + 2]) * srow * s4.z,
-                                     __uint_as_float(v[4 * j + 3]) * srow * s4.w);
+          for (int j = 0; j < 8; ++j) {
+            const float4 s4 = __ldg(swv + j);
+            p[2 * j] = pack_bf16x2(__uint_as_float(v[4 * j]) * srow * s4.x,
+                                   __uint_as_float(v[4 * j + 1]) * srow * s4.y);
+            p[2 * j + 1] = pack_bf16x2(__uint_as_float(v[4 * j + 2]) * srow * s4.z,
+                                       __uint_as_float(v[4 * j + 3]) * srow * s4.w);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(yrow + col0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+        } else {
+          // the ragged edge: one element at a time
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = col0 + j;
+            if (col < N)
+              yrow[col] = __float2bfloat16_rn(__uint_as_float(v[j]) * srow * __ldg(sw + col));
+          }
         }
-        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
       }
       tc::fence_before_sync();
       __syncwarp();
@@ -209,7 +226,7 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
       return RF_ERR_CUDA;
     attr_set = true;
   }
-  const int tiles = (M / BM) * (N / BN);
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int sms = tc::sm_count();
   const int grid = sms > 0 && sms < tiles ? sms : tiles;
   fp8_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sx, sw,

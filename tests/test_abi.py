@@ -104,14 +104,20 @@ def test_topk_validation(lib):
 
 def test_quant_gemm_validation(lib):
     f = lib.rf_absmax_quant_fp8_gemm
-    args = lambda **o: [o.get("x", FAKE), o.get("M", 256), o.get("K", 512), FAKE, FAKE,
-                        o.get("N", 256), FAKE, FAKE, FAKE, NULL]
+    args = lambda **o: [o.get("x", FAKE), o.get("M", 256), o.get("K", 512), FAKE,
+                        o.get("sw", FAKE), o.get("N", 256), FAKE, FAKE, FAKE, NULL]
+    # every call below is rejected before a launch (ragged M and N are
+    # supported, so they are only combined with a rejected argument)
     assert f(*args(x=NULL)) == 1
     assert f(*args(M=0)) == 1
     assert f(*args(K=100)) == 2
-    assert f(*args(N=100)) == 2
-    assert f(*args(M=100)) == 2
+    assert f(*args(K=40, N=100, M=100)) == 2
+    assert f(*args(K=65552)) == 2
     assert f(*args(x=ODD)) == 3
+    assert f(*args(sw=ODD, N=100)) == 3
+    g = lib.rf_fp8_gemm_scaled
+    assert g(FAKE, FAKE, FAKE, ODD, 100, 300, 64, FAKE, NULL) == 3
+    assert g(FAKE, FAKE, FAKE, FAKE, 100, 300, 24, FAKE, NULL) == 2
     q = lib.rf_absmax_quant_e4m3
     assert q(NULL, 4, 64, FAKE, FAKE, NULL) == 1
     assert q(FAKE, 4, 60, FAKE, FAKE, NULL) == 2

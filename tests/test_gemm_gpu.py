@@ -6,7 +6,7 @@ the same codes (which are first checked bit-exact against the oracle's own
 quantisation).  Y is bf16: |g - r| <= 2e-2 + 1e-2 |r|.
 
 Cases: one tile with one K block; several tiles and K blocks (the shared
-memory ring wraps); more tiles than SMs (persistent loop, both TMEM
+memory ring wraps); ragged M, N and K on every edge; more tiles than SMs (persistent loop, both TMEM
 accumulators reused); identity weights (Y = dequantised X * sw); the full
 workload X [4096 x 7168] with Wq [4096 x 7168], compared in full.
 """
@@ -50,6 +50,14 @@ def check(rf, M, K, N, seed, what):
                                    (384, 640, 768)])
 def test_small(rf, M, K, N):
     check(rf, M, K, N, seed=M + K + N, what=f"M={M} K={K} N={N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 16, 1), (1, 16, 8), (3, 48, 5), (130, 144, 300),
+                                   (77, 7184, 5), (200, 16, 264), (513, 1040, 1000), (129, 2064, 257)])
+def test_ragged(rf, M, K, N):
+    # partial tiles on every edge: rows past M, columns past N, a last K block
+    # shorter than 128 bytes; N not a multiple of 8 takes the element-wise stores
+    check(rf, M, K, N, seed=M * 7 + K + N, what=f"ragged M={M} K={K} N={N}")
 
 
 def test_more_tiles_than_sms(rf):

@@ -81,7 +81,8 @@ rf_status rf_attn_prefill(const void* q, const void* k, const void* v, int B, in
                           int causal, float scale, void* out, float* lse, void* stream) {
   if (!q || !k || !v || !out) return RF_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || N <= 0 || D <= 0 || !isfinite(scale)) return RF_ERR_INVALID_ARG;
-  if (D != 128 || N % 128 != 0) return RF_ERR_UNSUPPORTED;
+  if (D != 128) return RF_ERR_UNSUPPORTED;
+  if ((long long)B * H * N >= (1ll << 31)) return RF_ERR_UNSUPPORTED;
   if (!rf::aligned16(q) || !rf::aligned16(k) || !rf::aligned16(v) || !rf::aligned16(out))
     return RF_ERR_MISALIGNED;
   return rf::launch_prefill(q, k, v, B, H, N, D, causal ? 1 : 0, scale, out, lse,

@@ -125,7 +125,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int NB = N / BM;                              // query (and key) tiles per head
+  const int NB = (N + BM - 1) / BM;                   // query (and key) tiles per head
   const int NP = (NB + 1) / 2;                        // tile pairs per head
   // head-major order, heaviest pair of each head first
   const int bh = (int)(blockIdx.x / NP);
@@ -262,6 +262,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 64; ++i)
           if (col0 + i > r) s[i] = -INFINITY;
+      } else if (!causal && j == NB - 1 && N % BN != 0) {
+        // keys past N in the last tile are the next head's rows (or TMA's
+        // zero fill): leave them out.  Under the causal mask they never count
+        // for a row that is stored.
+        const int kmax = N - j * BN;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (col0 + i >= kmax) s[i] = -INFINITY;
       }
       // partial max of this half (raw scores; scale_log2 > 0 is applied later)
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -341,7 +349,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         const float lt = sh->l_part[x][0][r] + sh->l_part[x][1][r];
         const float inv = 1.f / lt;
         const int grow = key0 + m_tile * BM + r;      // global query row
-        __nv_bfloat16* orow = out + (size_t)grow * HD + col0;
+        const bool row_in = m_tile * BM + r < N;      // rows past N belong to no query
+        __nv_bfloat16* orow = out + (size_t)(row_in ? grow : key0) * HD + col0;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
@@ -353,11 +362,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv,
                                  __uint_as_float(v[2 * i + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          if (row_in) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
         }
-        if (lse != nullptr && half == 0) lse[grow] = (m_ref + log2f(lt)) * kLn2;
+        if (lse != nullptr && half == 0 && row_in) lse[grow] = (m_ref + log2f(lt)) * kLn2;
       }
     }
   }
@@ -392,7 +403,7 @@ rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int
       return RF_ERR_CUDA;
     attr_set = true;
   }
-  const int NB = N / BM;
+  const int NB = (N + BM - 1) / BM;
   const unsigned grid = (unsigned)(B * H) * (unsigned)((NB + 1) / 2);
   prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(out),
                                                    lse, N, causal, scale * kLog2e);

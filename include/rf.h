@@ -165,8 +165,10 @@ rf_status rf_mla_decode_split(const void* q, const void* c, int B, int H, int L,
  *   scale     score scale (1/sqrt(D))
  *   out       [B, H, N, D]  bf16 out
  *   lse       [B, H, N]     fp32 out (m + ln l, natural log), may be NULL
+ * Any N >= 1: the last query and key tiles of a head are partial (keys past
+ * N are left out, rows past N are not stored).
  * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
- * RF_ERR_UNSUPPORTED unless D = 128 and N % 128 == 0.
+ * RF_ERR_UNSUPPORTED unless D = 128 and B*H*N < 2^31.
  */
 rf_status rf_attn_prefill(const void* q, const void* k, const void* v,
                           int B, int H, int N, int D, int causal, float scale,

@@ -3,7 +3,8 @@ through the C ABI.  out is bf16 (|g - r| <= 2e-2 + 1e-2 |r|); lse is fp32
 (|g - r| <= 2e-3 |r| + 1e-6).
 
 Cases: one tile (N = 128) causal and not; several key tiles so the K/V ring
-and the two S buffers wrap; several batches and heads; peaked scores (large
+and the two S buffers wrap; ragged lengths (N = 1 … 1000, not multiples of
+128) causal and not; several batches and heads; peaked scores (large
 scale) that move the running max often; the full workload B=4, H=32,
 N=8192 with sampled rows compared one by one, and its closed form (causal
 row 0 equals V row 0 exactly).
@@ -53,6 +54,14 @@ def test_single_tile(rf, causal):
 @pytest.mark.parametrize("causal", [True, False])
 def test_several_key_tiles(rf, N, causal):
     check_all(rf, 1, 2, N, causal, seed=N)
+
+
+@pytest.mark.parametrize("N", [1, 77, 129, 200, 333, 1000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_lengths(rf, N, causal):
+    # a partial last tile: its keys past N are the next head's rows (or the
+    # zero fill past the tensor) and must be left out; rows past N not stored
+    check_all(rf, 2, 2, N, causal, seed=N + 3)
 
 
 def test_batches_and_heads(rf):

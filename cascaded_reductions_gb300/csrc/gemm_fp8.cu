@@ -15,7 +15,10 @@
 //               row, 32 columns at a time), scale by sx[row] * sw[col],
 //               round to bf16, store; then hand the accumulator back, so the
 //               next tile's MMAs overlap this tile's epilogue.
-// Output tiles are 128 x 256; CTAs walk tiles t = blockIdx.x + i*gridDim.x.
+// Output tiles are 128 x 256; CTAs walk work items t = blockIdx.x + i*gridDim.x.
+// When the tiles left after the whole waves fit into one wave as halves,
+// those tiles run as 128 x 128 halves (N = 128 MMAs), so the last wave is a
+// half-tile wave rather than a sparse whole-tile one.
 // Every barrier wait is bounded (see tc_common.cuh).
 
 #include <cuda_bf16.h>
@@ -50,8 +53,9 @@ static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB of shared memory a CTA 
 
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const float* __restrict__ sx, const float* __restrict__ sw,
-                __nv_bfloat16* __restrict__ y, int M, int N, int K) {
+                const __grid_constant__ CUtensorMap tmBh, const float* __restrict__ sx,
+                const float* __restrict__ sw, __nv_bfloat16* __restrict__ y, int M, int N, int K,
+                int full_items, int num_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -61,8 +65,20 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   // ragged edges: the tensor maps zero-fill rows past M / N and columns past
   // K (an e4m3 zero adds nothing), the epilogue masks what it stores
   const int tiles_n = (N + BN - 1) / BN;
-  const int num_tiles = ((M + BM - 1) / BM) * tiles_n;
   const int num_k = (K + BK - 1) / BK;
+  // work item i: a 128 x 256 tile for i < full_items, else half of one of
+  // the remaining tiles (128 x 128), so the last wave is a half-tile wave
+  auto item = [&](int i, int& tm, int& col0, int& width) {
+    int tile = i, half = 0;
+    width = BN;
+    if (i >= full_items) {
+      tile = full_items + ((i - full_items) >> 1);
+      half = (i - full_items) & 1;
+      width = BN / 2;
+    }
+    tm = tile / tiles_n;
+    col0 = (tile - tm * tiles_n) * BN + half * (BN / 2);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -77,6 +93,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     tc::fence_barrier_init();
     tc::prefetch_tmap(&tmA);
     tc::prefetch_tmap(&tmB);
+    tc::prefetch_tmap(&tmBh);
   }
   if (warp == 1) tc::tmem_alloc(&sh->tmem_base, TMEM_COLS);
   tc::fence_before_sync();
@@ -89,16 +106,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // ------------------------------------------------ TMA producer ----
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x) {
-        const int tm = tile / tiles_n, tn = tile - (tile / tiles_n) * tiles_n;
+      for (int i = blockIdx.x; i < num_items && !*abort; i += gridDim.x) {
+        int tm, col0, width;
+        item(i, tm, col0, width);
+        const bool half = width != BN;
         for (int kb = 0; kb < num_k; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!tc::mbar_wait(&sh->empty[s], ph ^ 1u, abort)) break;
           uint8_t* a = smem + (size_t)s * STAGE_BYTES;
-          tc::mbar_arrive_expect_tx(&sh->full[s], STAGE_BYTES);
+          tc::mbar_arrive_expect_tx(&sh->full[s], half ? A_BYTES + B_BYTES / 2 : STAGE_BYTES);
           tc::tma_load_2d(a, &tmA, &sh->full[s], kb * BK, tm * BM);
-          tc::tma_load_2d(a + A_BYTES, &tmB, &sh->full[s], kb * BK, tn * BN);
+          tc::tma_load_2d(a + A_BYTES, half ? &tmBh : &tmB, &sh->full[s], kb * BK, col0);
         }
       }
       // On an abort, let the copies already issued land before the CTA exits.
@@ -114,9 +133,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer ----
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_e4m3_f32(BM, BN);
+      constexpr uint32_t idesc_full = tc::idesc_e4m3_f32(BM, BN);
+      constexpr uint32_t idesc_half = tc::idesc_e4m3_f32(BM, BN / 2);
       uint32_t it = 0, t = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x, ++t) {
+      for (int i = blockIdx.x; i < num_items && !*abort; i += gridDim.x, ++t) {
+        const uint32_t idesc = i < full_items ? idesc_full : idesc_half;
         const int buf = t & 1;
         const uint32_t bph = (t >> 1) & 1u;
         if (!tc::mbar_wait(&sh->acc_empty[buf], bph ^ 1u, abort)) break;
@@ -151,20 +172,21 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     const int r = quarter * 32 + lane;         // row within the tile
     uint32_t t = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
+    for (int i = blockIdx.x; i < num_items; i += gridDim.x, ++t) {
       const int buf = t & 1;
       const uint32_t bph = (t >> 1) & 1u;
       if (!tc::mbar_wait(&sh->acc_full[buf], bph, abort)) break;
       tc::fence_after_sync();
-      const int tm = tile / tiles_n, tn = tile - (tile / tiles_n) * tiles_n;
+      int tm, tcol0, width;
+      item(i, tm, tcol0, width);
       const int row = tm * BM + r;
       const bool row_in = row < M;
       const float srow = row_in ? sx[row] : 0.f;
       __nv_bfloat16* yrow = y + (size_t)(row_in ? row : 0) * N;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = tn * BN + c * 32;
+      for (int c = 0; c < width / 32; ++c) {
+        const int col0 = tcol0 + c * 32;
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(taddr + (uint32_t)(c * 32), v);   // whole warp, every row
         tc::tmem_ld_wait();
@@ -213,11 +235,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
 rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                           int M, int N, int K, void* y, cudaStream_t st) {
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tbh;
   if (!tc::make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
                         (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
-                        (uint64_t)K, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B))
+                        (uint64_t)K, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
+                        (uint64_t)K, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
@@ -229,8 +253,19 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int sms = tc::sm_count();
   const int grid = sms > 0 && sms < tiles ? sms : tiles;
-  fp8_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, sx, sw,
-                                                     static_cast<__nv_bfloat16*>(y), M, N, K);
+  // Wave shaping: when the tiles left after the full waves fit into one wave
+  // as halves, run them as 128 x 128 halves (e.g. 512 tiles on 152 SMs: 3
+  // waves of whole tiles + one wave of 112 halves instead of a fourth wave of
+  // 56 whole tiles).
+  const int waves = tiles / grid, rem = tiles - waves * grid;
+  int full_items = tiles, num_items = tiles;
+  if (waves >= 1 && rem > 0 && 2 * rem <= grid) {
+    full_items = waves * grid;
+    num_items = full_items + 2 * rem;
+  }
+  fp8_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tbh, sx, sw,
+                                                     static_cast<__nv_bfloat16*>(y), M, N, K,
+                                                     full_items, num_items);
   return launch_status();
 }
 

@@ -60,6 +60,13 @@ def test_ragged(rf, M, K, N):
     check(rf, M, K, N, seed=M * 7 + K + N, what=f"ragged M={M} K={K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(2560, 272, 2048), (2500, 272, 2000)])
+def test_half_tile_last_wave(rf, M, K, N):
+    # 160 output tiles on 152 SMs: one whole wave, then the 8 tiles left run
+    # as 16 half tiles (128 x 128); the second shape also has ragged edges
+    check(rf, M, K, N, seed=M + N, what=f"half-tile wave M={M} K={K} N={N}")
+
+
 def test_more_tiles_than_sms(rf):
     # 32 x 12 = 384 output tiles: every CTA runs several tiles
     check(rf, 4096, 256, 3072, seed=11, what="persistent")

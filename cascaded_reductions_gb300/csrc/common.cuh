@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "rf.h"
 
 namespace rf {
@@ -80,6 +82,22 @@ struct Chunk<Bf16Tag> {
 __device__ __forceinline__ float ref_of(float m) { return m == -INFINITY ? 0.f : m; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Opt a kernel into `bytes` of dynamic shared memory on the current device,
+// once per device: the attribute belongs to the device's context, so each
+// kernel keeps one flag bit per device (up to 64), set atomically.
+template <typename Kernel>
+inline rf_status smem_attr(Kernel kern, size_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RF_ERR_CUDA;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return RF_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return RF_ERR_CUDA;
+  done.fetch_or(bit, std::memory_order_release);
+  return RF_OK;
+}
 
 inline rf_status launch_status() {
   cudaError_t e = cudaGetLastError();

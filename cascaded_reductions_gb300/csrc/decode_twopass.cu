@@ -146,13 +146,8 @@ rf_status launch_twopass_t(const void* q, const void* k, const void* v, int R, i
   constexpr int WARPS = 8, U = 8;
   const size_t smem = (size_t)(seg_len > 0 ? seg_len : 1) * sizeof(float);
   auto kern = decode_twopass_kernel<T, WARPS, U>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kTwopassMaxSeg * (int)sizeof(float)) != cudaSuccess)
-      return RF_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (smem_attr(kern, kTwopassMaxSeg * sizeof(float), attr) != RF_OK) return RF_ERR_CUDA;
   const unsigned grid = (unsigned)R * (unsigned)S;
   kern<<<grid, WARPS * 32, smem, st>>>(static_cast<const uint8_t*>(q),
                                        static_cast<const uint8_t*>(k),

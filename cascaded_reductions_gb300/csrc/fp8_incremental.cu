@@ -295,13 +295,8 @@ rf_status launch_fp8_incremental(const void* x, const uint8_t* wq, const float* 
       !tc::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K, BK, 256, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fp8_incremental_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-      return RF_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (smem_attr(fp8_incremental_kernel, SMEM_BYTES, attr) != RF_OK) return RF_ERR_CUDA;
   const unsigned grid = (unsigned)(M / BM) * (unsigned)(N / BN);
   fp8_incremental_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(
       tx, tw, sw, static_cast<__nv_bfloat16*>(y), sx_final, M, N, K);

@@ -243,13 +243,8 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
       !tc::make_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-      return RF_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (smem_attr(fp8_gemm_kernel, SMEM_BYTES, attr) != RF_OK) return RF_ERR_CUDA;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int sms = tc::sm_count();
   const int grid = sms > 0 && sms < tiles ? sms : tiles;

@@ -494,13 +494,8 @@ rf_status launch_hg(const void* q, const void* c, int B, int H, int L, int S, fl
                         BK, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
   auto kern = mla_decode_kernel<HG>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Layout<HG>::SMEM) != cudaSuccess)
-      return RF_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (smem_attr(kern, Layout<HG>::SMEM, attr) != RF_OK) return RF_ERR_CUDA;
   const int seg = (L + S - 1) / S;
   const long long units = (long long)B * (H / HG) * S;
   const long long sms = tc::sm_count();

@@ -396,13 +396,8 @@ rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int
       !tc::make_tmap_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, HD, rows, stride, 64, BN,
                         CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-      return RF_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr{0};
+  if (smem_attr(prefill_kernel, SMEM_BYTES, attr) != RF_OK) return RF_ERR_CUDA;
   const int NB = (N + BM - 1) / BM;
   const unsigned grid = (unsigned)(B * H) * (unsigned)((NB + 1) / 2);
   prefill_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(tq, tk, tv, static_cast<__nv_bfloat16*>(out),

@@ -81,6 +81,39 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// fp32 pairs in one 64-bit register for the packed FMA / add of sm_100+
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float hi_f32(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // load a 128x128 bf16 tile as two 128-byte-wide boxes
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
                                           int row) {
@@ -271,10 +304,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         for (int i = 0; i < 64; ++i)
           if (col0 + i >= kmax) s[i] = -INFINITY;
       }
-      // partial max of this half (raw scores; scale_log2 > 0 is applied later)
+      // partial max of this half (raw scores; scale_log2 > 0 is applied
+      // later), three-input max: half the instructions of a two-input chain
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+      for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], s[i], s[i + 1]);
       const float pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       // exchange with the other half of the row
       sh->pmax[x][j & 1][half][r] = pm;
@@ -292,20 +326,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       const float alpha = ex2(m_ref - m_new);       // 0 on the first tile, 1 when not moved
       l *= alpha;
       // this thread's 64 keys of P into its 32 columns of S (two bf16 per column)
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // arguments and row sums on pairs of keys (packed fp32x2 FMA and add)
+      uint64_t sum2[2] = {0ull, 0ull};
+      const uint64_t sl2 = pack_f32x2(scale_log2, scale_log2);
+      const uint64_t nm2 = pack_f32x2(-m_new, -m_new);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(s[c * 32 + 2 * i], scale_log2, -m_new));
-          const float p1 = ex2(fmaf(s[c * 32 + 2 * i + 1], scale_log2, -m_new));
-          sum[i & 3] += p0 + p1;
+          const uint64_t a = fma_f32x2(pack_f32x2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2, nm2);
+          const float p0 = ex2(lo_f32(a));
+          const float p1 = ex2(hi_f32(a));
+          const uint64_t p = pack_f32x2(p0, p1);
+          sum2[i & 1] = add_f32x2(sum2[i & 1], p);
           w[i] = pack_bf16x2(p0, p1);
         }
         tc::tmem_st_32x32b_x16(lane_base + s_col(x) + (uint32_t)(half * 32 + c * 16), w);
       }
-      l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      {
+        const uint64_t t2 = add_f32x2(sum2[0], sum2[1]);
+        l += lo_f32(t2) + hi_f32(t2);
+      }
       m_ref = m_new;
       // O must hold every earlier P V before it is rescaled
       if (j > 0) {

@@ -49,6 +49,7 @@ _SIGNATURES = {
     "rf_attn_decode_split_twopass": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P]),
     "rf_incremental_quant_fp8_gemm": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "rf_mla_decode_split": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "rf_selftest_wait_timeout": (_I, [_P, _P]),
 }
 
 
@@ -311,6 +312,12 @@ def rf_incremental_quant_fp8_gemm(x, wq, sw, y, sx_final=None, stream=None):
     _check(_lib.rf_incremental_quant_fp8_gemm(_ptr(x), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
                                               _ptr(sx_final), _stream(stream)),
            "rf_incremental_quant_fp8_gemm")
+
+
+def rf_selftest_wait_timeout(waited_ms, stream=None):
+    """waited_ms: int32 CUDA tensor of one element; the timeout shows up in rf_device_error()."""
+    _need(waited_ms, torch.int32, "waited_ms", (1,))
+    _check(_lib.rf_selftest_wait_timeout(_ptr(waited_ms), _stream(stream)), "rf_selftest_wait_timeout")
 
 
 def rf_device_error(stream=None):

@@ -202,3 +202,8 @@ rf_status rf_device_error(int* status, void* stream) {
 }
 
 }  // extern "C"
+
+rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream) {
+  if (!waited_ms) return RF_ERR_INVALID_ARG;
+  return rf::launch_selftest_wait_timeout(waited_ms, as_stream(stream));
+}

@@ -136,6 +136,8 @@ rf_status fp8_incremental_take_status(int* status);
 rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, int S, float scale,
                             float* seg_m, float* seg_l, float* seg_acc, cudaStream_t st);
 rf_status mla_take_status(int* status);
+rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st);
+rf_status selftest_take_status(int* status);
 rf_status read_device_error(int* status, cudaStream_t st);
 // read and clear the bounded-wait status word of each tensor-core kernel file
 rf_status gemm_take_status(int* status);

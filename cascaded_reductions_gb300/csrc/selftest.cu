@@ -1,0 +1,47 @@
+// Self-test of the bounded waits the tensor-core kernels use.
+//
+// One thread waits on a shared-memory mbarrier that nothing ever arrives on,
+// through the same tc::mbar_wait every pipeline wait in this library uses.
+// The wait gives up after its limit (kWaitLimitNs), sets the CTA's abort
+// flag, records RF_ERR_TIMEOUT in this translation unit's status word and
+// the kernel returns normally: no fault, no trap, no hang, and the context
+// stays usable.  The host reads the status through rf_device_error.
+
+#include "tc_common.cuh"
+
+namespace rf {
+namespace {
+
+__global__ void wait_timeout_kernel(int* __restrict__ waited_ms) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = tc::globaltimer_ns();
+    const bool completed = tc::mbar_wait(&bar, 0, &abort_flag);   // nothing arrives
+    const unsigned long long dt = tc::globaltimer_ns() - t0;
+    *waited_ms = completed ? -1 : (int)(dt / 1000000ull);
+  }
+}
+
+}  // namespace
+
+rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(waited_ms);
+  return launch_status();
+}
+
+rf_status selftest_take_status(int* status) {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
+  *status = v;
+  return RF_OK;
+}
+
+}  // namespace rf

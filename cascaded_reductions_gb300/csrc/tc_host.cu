@@ -46,11 +46,17 @@ int sm_count() {
 
 rf_status read_device_error(int* status, cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return RF_ERR_CUDA;
-  int a = 0, b = 0, c = 0, d = 0;
-  if (gemm_take_status(&a) != RF_OK || prefill_take_status(&b) != RF_OK ||
-      fp8_incremental_take_status(&c) != RF_OK || mla_take_status(&d) != RF_OK)
+  int st_words[5] = {0, 0, 0, 0, 0};
+  if (gemm_take_status(&st_words[0]) != RF_OK || prefill_take_status(&st_words[1]) != RF_OK ||
+      fp8_incremental_take_status(&st_words[2]) != RF_OK || mla_take_status(&st_words[3]) != RF_OK ||
+      selftest_take_status(&st_words[4]) != RF_OK)
     return RF_ERR_CUDA;
-  *status = a != RF_OK ? a : (b != RF_OK ? b : (c != RF_OK ? c : d));
+  *status = RF_OK;
+  for (int w : st_words)
+    if (w != RF_OK) {
+      *status = w;
+      break;
+    }
   return RF_OK;
 }
 

@@ -322,6 +322,21 @@ rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, i
                         float eps, float* y, int level, float* work, void* stream);
 
 /*
+ * rf_selftest_wait_timeout -- a self-test of the bounded waits (the pages
+ * have no counterpart: this checks this library's failure detection).  One
+ * thread of a one-CTA kernel waits on a shared-memory barrier that nothing
+ * arrives on, through the same bounded wait every tensor-core pipeline wait
+ * uses; after the limit (about 1 s) the wait gives up, the kernel records
+ * RF_ERR_TIMEOUT for rf_device_error and returns normally (no fault, no
+ * hang; the context stays usable).
+ *   waited_ms  [1] int32, device memory, out: how long the wait lasted in
+ *              milliseconds, or -1 if it completed (it never should)
+ * Errors: RF_ERR_INVALID_ARG for a null pointer.  The timeout itself is
+ * reported by the next rf_device_error call, not by this call.
+ */
+rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream);
+
+/*
  * rf_device_error -- status of the bounded on-device waits.  The
  * tensor-core kernels wait on shared-memory barriers with an iteration
  * limit; a wait that runs out records RF_ERR_TIMEOUT in a device word and

@@ -211,3 +211,7 @@ def test_merge_accepts_the_mla_value_width(lib):
     f = lib.rf_state_merge
     # D = 512 passes validation and fails only on the misaligned output
     assert f(FAKE, FAKE, FAKE, 4, 8, 512, ODD, 1, NULL, NULL) == 3
+
+
+def test_selftest_validation(lib):
+    assert lib.rf_selftest_wait_timeout(NULL, NULL) == 1

@@ -1,5 +1,5 @@
 """Single-row cascade oracles: safe softmax of a row, variance, moment of
-inertia, layer normalisation.
+inertia, layer normalisation, RMS normalisation.
 
 RedFuser episode transcript, cue 47: the paper measures safe softmax on rows
 of 1K to 8K elements at several fusion levels, and also runs variance and
@@ -63,3 +63,15 @@ def layer_norm(x, gamma, beta, eps):
     mean, var = row_variance(x)
     return ((x - mean[:, None]) / np.sqrt(var[:, None] + eps) * np.asarray(gamma, np.float64)
             + np.asarray(beta, np.float64))
+
+
+def rms_norm(x, gamma, eps):
+    """x [R, n], gamma [n] -> y [R, n].
+
+    Pass 1: the mean of squares ms = sum x^2 / n; pass 2: y = x / sqrt(ms +
+    eps) * gamma (the normalisation needs the finished reduction; bookshelf
+    explainer, "Problem": normalisation layers are cascaded reductions).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = (x * x).sum(axis=1) / x.shape[1]
+    return x / np.sqrt(ms[:, None] + eps) * np.asarray(gamma, np.float64)

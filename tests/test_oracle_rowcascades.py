@@ -89,3 +89,24 @@ def test_layer_norm_matches_torch_and_closed_form():
     z = rc.layer_norm(x, np.ones(777), np.zeros(777), 0.0)
     np.testing.assert_allclose(z.mean(axis=1), 0.0, atol=1e-12)
     np.testing.assert_allclose(z.var(axis=1), 1.0, rtol=1e-12)
+
+
+def test_rms_norm_matches_torch_closed_forms_and_brute_force():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((5, 333)) * 2 - 0.5
+    g = rng.standard_normal(333)
+    y = rc.rms_norm(x, g, 1e-6)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (333,), torch.from_numpy(g), 1e-6)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=1e-11, atol=1e-12)
+    # a constant row c normalises to sign(c) when eps = 0; scale invariance
+    c = rc.rms_norm(np.full((2, 64), -3.5), np.ones(64), 0.0)
+    np.testing.assert_allclose(c, -1.0, rtol=1e-15)
+    np.testing.assert_allclose(rc.rms_norm(x * 7.25, g, 0.0), rc.rms_norm(x, g, 0.0), rtol=1e-12)
+    # unit gain: every row has mean square ms/(ms + eps), 1 for eps = 0
+    z = rc.rms_norm(x, np.ones(333), 0.0)
+    np.testing.assert_allclose((z * z).mean(axis=1), 1.0, rtol=1e-12)
+    # brute force on a tiny row
+    row, gam, eps = [1.0, -2.0, 0.5], [2.0, 1.0, -1.0], 0.25
+    ms = sum(v * v for v in row) / 3
+    want = [row[i] / math.sqrt(ms + eps) * gam[i] for i in range(3)]
+    np.testing.assert_allclose(rc.rms_norm(np.array([row]), np.array(gam), eps)[0], want, rtol=1e-14)

@@ -20,8 +20,10 @@ The same line carries:
                 core);
   clocks        nvidia-smi samples taken during the timed region;
   paths         the other cascades (single-row fp32 decode, both routing
-                shapes, quantisation, FP8 GEMM, causal prefill), each timed
-                on its own with its roofline (informational).
+                shapes, quantisation, FP8 GEMM, causal prefill, MLA decode,
+                the single-row cascades at every fusion level, LayerNorm and
+                RMSNorm) and the incremental vs non-incremental decode
+                ablations, each timed on its own with its roofline.
 
 ``--impl reference`` times the CPU oracle alone as the reference arm (same
 metric, unit and config; each step is a bounded sample of rows).
@@ -330,13 +332,14 @@ def roofline(bound, achieved, peak, unit, traffic):
             "frac": round(achieved / peak, 4), "traffic": traffic}
 
 
-def decode_ablation(torch, rf, peaks, q, K, V, scale):
-    """Incremental vs non-incremental split-KV decode on the headline inputs,
-    for every segment count S: time of the segment-state kernel alone."""
+def decode_ablation(torch, rf, peaks, q, K, V, scale, segments=(1, 2, 4, 8, 16, 32, 64),
+                    workload=None):
+    """Incremental vs non-incremental split-KV decode, for every segment count
+    S: time of the segment-state kernel alone."""
     R, L, D = K.shape
-    kv_bytes = 2 * R * L * D * 2
+    kv_bytes = 2 * K.numel() * K.element_size()
     res = {}
-    for S in (1, 2, 4, 8, 16, 32, 64):
+    for S in segments:
         sm = torch.empty(R, S, device="cuda")
         sl = torch.empty(R, S, device="cuda")
         sa = torch.empty(R, S, D, device="cuda")
@@ -360,9 +363,22 @@ def decode_ablation(torch, rf, peaks, q, K, V, scale):
             row[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
                          "frac": round(gbs / peaks["hbm_gbs"], 4)}
         res[f"S{S}"] = row
-    res["workload"] = ("segment-state kernel only, B=32 H=32 L=32768 D=128 bf16; the "
-                       "non-incremental kernel keeps a segment's scores in shared memory "
-                       "(segments of at most 16384 keys)")
+    res["workload"] = workload or (
+        "segment-state kernel only, B=32 H=32 L=32768 D=128 bf16; the non-incremental kernel "
+        "keeps a segment's scores in shared memory (segments of at most 16384 keys)")
+    return res
+
+
+def decode_ablation_short(torch, rf, peaks):
+    """The same comparison on short per-block sequences: 16384 rows of L=512
+    keys, D=64 fp32 (BERT-base's head width and sequence length), S = 1..8
+    (512 down to 64 keys per block)."""
+    import synthetic_inputs as si
+    q, K, V = si.decode_inputs(16384, 512, 64, torch.float32, seed=7, device="cuda")
+    res = decode_ablation(torch, rf, peaks, q, K, V, si.decode_scale(64), segments=(1, 2, 4, 8),
+                          workload="segment-state kernel only, 16384 rows x L=512 keys, D=64 fp32 "
+                                   "(BERT-base head width and sequence length); K/V 4.3 GB > L2")
+    del q, K, V
     return res
 
 
@@ -594,10 +610,15 @@ def path_row_cascades(torch, rf, peaks):
     for lvl, nm in ((0, "unfused"), (1, "fused")):
         ms = time_graph(torch, [lambda: rf.rf_layer_norm(xl, gam, bet, 1e-5, yl, lvl, wl)] * 5, 5)
         res["layer_norm"][nm] = entry(ms, 2 * xl.numel() * 4)
+    res["rms_norm"] = {}
+    wr = torch.empty(16384, device="cuda")
+    for lvl, nm in ((0, "unfused"), (1, "fused")):
+        ms = time_graph(torch, [lambda: rf.rf_rms_norm(xl, gam, 1e-6, yl, lvl, wr)] * 5, 5)
+        res["rms_norm"][nm] = entry(ms, 2 * xl.numel() * 4)
     del xl, yl
     res["workload"] = ("row softmax R = 2^26/n rows of n fp32 (read + write counted); variance "
                        "x [16384, 4096]; moment of inertia mass [4096, 4096] + pos [4096, 3, 4096]; "
-                       "layer norm x, y [16384, 4096] (read + write counted); "
+                       "layer norm and RMS norm x, y [16384, 4096] (read + write counted); "
                        "CUDA graphs of 5 calls, inputs larger than L2")
     return res
 
@@ -633,6 +654,7 @@ def run_rf(args):
                "prefill": lambda: path_prefill(torch, rf, peaks),
                "mla": lambda: path_mla(torch, rf, peaks, args.mla_segments),
                "rows": lambda: path_row_cascades(torch, rf, peaks),
+               "ablation_short": lambda: decode_ablation_short(torch, rf, peaks),
                "ablation": lambda: decode_ablation(
                    torch, rf, peaks, *si.decode_inputs(1024, 32768, 128, torch.bfloat16, seed=2,
                                                        device="cuda"), si.decode_scale(128))}
@@ -722,6 +744,7 @@ def run_rf(args):
     if world == 1 and not args.decode_only:
         paths["decode_incremental_vs_non_incremental"] = decode_ablation(torch, rf, peaks, q, K, V,
                                                                          scale)
+        paths["decode_incremental_vs_non_incremental_short"] = decode_ablation_short(torch, rf, peaks)
         del q, K, V
         torch.cuda.empty_cache()
         for name, fn in (("single_row_decode_f32", lambda: path_single_row(torch, rf, peaks)),
@@ -815,7 +838,7 @@ def main():
                     help="decode rows instead of B*H=1024 (small cases for ncu captures)")
     ap.add_argument("--decode-only", action="store_true", help="skip the other cascades")
     ap.add_argument("--only", choices=["single_row", "routing_256", "routing_64", "quant", "gemm", "mla",
-                                       "prefill", "rows", "ablation"],
+                                       "prefill", "rows", "ablation", "ablation_short"],
                     help="time one other cascade alone")
     ap.add_argument("--mla-segments", type=int, default=0,
                     help="with --only mla: time this segment count alone (profiler captures)")

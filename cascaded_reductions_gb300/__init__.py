@@ -50,6 +50,7 @@ _SIGNATURES = {
     "rf_incremental_quant_fp8_gemm": (_I, [_P, _I, _I, _P, _P, _I, _P, _P, _P]),
     "rf_mla_decode_split": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_P, _P]),
+    "rf_rms_norm": (_I, [_P, _P, _I, _I, _F, _P, _I, _P, _P]),
 }
 
 
@@ -297,6 +298,18 @@ def rf_layer_norm(x, gamma, beta, eps, y, level, work=None, stream=None):
         _need(work, torch.float32, "work", (2 * R,))
     _check(_lib.rf_layer_norm(_ptr(x), _ptr(gamma), _ptr(beta), R, n, float(eps), _ptr(y),
                               int(level), _ptr(work), _stream(stream)), "rf_layer_norm")
+
+
+def rf_rms_norm(x, gamma, eps, y, level, work=None, stream=None):
+    """x, y [R, n] fp32; gamma [n]; level RF_FUSE_NONE needs work [R] fp32."""
+    R, n = x.shape
+    _need(x, torch.float32, "x")
+    _need(gamma, torch.float32, "gamma", (n,))
+    _need(y, torch.float32, "y", (R, n))
+    if work is not None:
+        _need(work, torch.float32, "work", (R,))
+    _check(_lib.rf_rms_norm(_ptr(x), _ptr(gamma), R, n, float(eps), _ptr(y), int(level), _ptr(work),
+                            _stream(stream)), "rf_rms_norm")
 
 
 def rf_incremental_quant_fp8_gemm(x, wq, sw, y, sx_final=None, stream=None):

@@ -185,6 +185,18 @@ rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, i
   return rf::launch_layer_norm(x, gamma, beta, R, n, eps, y, level, work, as_stream(stream));
 }
 
+rf_status rf_rms_norm(const float* x, const float* gamma, int R, int n, float eps, float* y,
+                      int level, float* work, void* stream) {
+  if (!x || !gamma || !y) return RF_ERR_INVALID_ARG;
+  rf_status s = check_row_args(R, n, level);
+  if (s != RF_OK) return s;
+  if (!(eps >= 0.f) || !isfinite(eps)) return RF_ERR_INVALID_ARG;
+  if (level == RF_FUSE_NONE && !work) return RF_ERR_INVALID_ARG;
+  if (level != RF_FUSE_NONE && n > 8192) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(x) || !rf::aligned16(y) || !rf::aligned16(gamma)) return RF_ERR_MISALIGNED;
+  return rf::launch_rms_norm(x, gamma, R, n, eps, y, level, work, as_stream(stream));
+}
+
 rf_status rf_incremental_quant_fp8_gemm(const void* x, int M, int K, const uint8_t* wq,
                                         const float* sw, int N, void* y, float* sx_final,
                                         void* stream) {

@@ -612,6 +612,66 @@ layernorm_apply_kernel(const float* __restrict__ x, const float* __restrict__ ga
   }
 }
 
+// ---------------------------------------------------------- RMS norm ----
+// fused: the row stays in registers (VPT float4 per thread); the sum of
+// squares is reduced across the block, then the same registers are scaled
+// by rsqrt(ms + eps) * gamma and written
+template <int VPT>
+__global__ void __launch_bounds__(TH)
+rmsnorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int n, float eps,
+                     float* __restrict__ y) {
+  __shared__ float red[NW];
+  const int n4 = n >> 2;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
+  float4* yr = reinterpret_cast<float4*>(y + (size_t)blockIdx.x * n);
+  float4 v[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * TH + threadIdx.x;
+    v[i] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
+  }
+  const float rs = rsqrtf(bsum(ss, red) / (float)n + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) {
+    const int c = i * TH + threadIdx.x;
+    if (c < n4) {
+      const float4 g = __ldg(g4 + c);
+      __stcs(yr + c, make_float4(v[i].x * rs * g.x, v[i].y * rs * g.y, v[i].z * rs * g.z,
+                                 v[i].w * rs * g.w));
+    }
+  }
+}
+
+// unfused: one kernel for the mean of squares, one that re-reads the row
+__global__ void __launch_bounds__(TH)
+meansq_kernel(const float* __restrict__ x, int n, float* __restrict__ ms_out) {
+  __shared__ float red[NW];
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
+  float s = 0.f;
+  for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    const float4 v = __ldcs(xr + c);
+    s += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
+  }
+  s = bsum(s, red);
+  if (threadIdx.x == 0) ms_out[blockIdx.x] = s / (float)n;
+}
+
+__global__ void __launch_bounds__(TH)
+rmsnorm_apply_kernel(const float* __restrict__ x, const float* __restrict__ gamma, int n, float eps,
+                     const float* __restrict__ ms, float* __restrict__ y) {
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
+  float4* yr = reinterpret_cast<float4*>(y + (size_t)blockIdx.x * n);
+  const float rs = rsqrtf(ms[blockIdx.x] + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+  for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    const float4 v = __ldcs(xr + c), g = __ldg(g4 + c);
+    __stcs(yr + c, make_float4(v.x * rs * g.x, v.y * rs * g.y, v.z * rs * g.z, v.w * rs * g.w));
+  }
+}
+
 template <int LEVEL>
 void launch_softmax_level(const float* x, int R, int n, float* y, cudaStream_t st) {
   const int vpt = (n / 4 + TH - 1) / TH;
@@ -650,6 +710,21 @@ rf_status launch_layer_norm(const float* x, const float* gamma, const float* bet
     else if (vpt <= 2) layernorm_fused_kernel<2><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
     else if (vpt <= 4) layernorm_fused_kernel<4><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
     else layernorm_fused_kernel<8><<<R, TH, 0, st>>>(x, gamma, beta, n, eps, y);
+  }
+  return launch_status();
+}
+
+rf_status launch_rms_norm(const float* x, const float* gamma, int R, int n, float eps, float* y,
+                          int level, float* work, cudaStream_t st) {
+  if (level == RF_FUSE_NONE) {
+    meansq_kernel<<<R, TH, 0, st>>>(x, n, work);
+    rmsnorm_apply_kernel<<<R, TH, 0, st>>>(x, gamma, n, eps, work, y);
+  } else {
+    const int vpt = (n / 4 + TH - 1) / TH;
+    if (vpt <= 1) rmsnorm_fused_kernel<1><<<R, TH, 0, st>>>(x, gamma, n, eps, y);
+    else if (vpt <= 2) rmsnorm_fused_kernel<2><<<R, TH, 0, st>>>(x, gamma, n, eps, y);
+    else if (vpt <= 4) rmsnorm_fused_kernel<4><<<R, TH, 0, st>>>(x, gamma, n, eps, y);
+    else rmsnorm_fused_kernel<8><<<R, TH, 0, st>>>(x, gamma, n, eps, y);
   }
   return launch_status();
 }

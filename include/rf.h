@@ -321,6 +321,21 @@ rf_status rf_moment_of_inertia(const float* mass, const float* pos, int R, int n
 rf_status rf_layer_norm(const float* x, const float* gamma, const float* beta, int R, int n,
                         float eps, float* y, int level, float* work, void* stream);
 
+/* rf_rms_norm -- y = x / sqrt(mean(x^2) + eps) * gamma per row: the mean of
+ * squares, then the normalisation that needs it (the bookshelf explainer's
+ * "Problem" section lists normalisation layers among the cascaded
+ * reductions).  RF_FUSE_NONE runs one kernel per stage, each reading the
+ * row; any other level runs the fused single-read kernel (the row stays in
+ * registers, n <= 8192).
+ *   x, y [R, n] fp32 (n % 4 == 0);  gamma [n] fp32;  eps >= 0
+ *   work [R] fp32 scratch for RF_FUSE_NONE (row mean of squares), else may be NULL
+ * Errors: RF_ERR_INVALID_ARG for null pointers, R, n <= 0, a level outside
+ * 0..3, a negative or non-finite eps, or RF_FUSE_NONE without work;
+ * RF_ERR_UNSUPPORTED for n % 4 != 0 or a fused call with n > 8192;
+ * RF_ERR_MISALIGNED unless x, y and gamma are 16-byte aligned. */
+rf_status rf_rms_norm(const float* x, const float* gamma, int R, int n, float eps, float* y,
+                      int level, float* work, void* stream);
+
 /*
  * rf_selftest_wait_timeout -- a self-test of the bounded waits (the pages
  * have no counterpart: this checks this library's failure detection).  One

@@ -215,3 +215,17 @@ def test_merge_accepts_the_mla_value_width(lib):
 
 def test_selftest_validation(lib):
     assert lib.rf_selftest_wait_timeout(NULL, NULL) == 1
+
+
+def test_rms_norm_validation(lib):
+    f = lib.rf_rms_norm
+    args = lambda **o: [o.get("x", FAKE), FAKE, o.get("R", 4), o.get("n", 64), F(o.get("eps", 1e-6)),
+                        FAKE, o.get("level", 1), o.get("work", NULL), NULL]
+    assert f(*args(x=NULL)) == 1
+    assert f(*args(R=0)) == 1
+    assert f(*args(eps=float("inf"))) == 1
+    assert f(*args(level=7)) == 1
+    assert f(*args(level=0)) == 1                    # unfused needs work
+    assert f(*args(n=66)) == 2
+    assert f(*args(n=8196)) == 2
+    assert f(*args(x=ODD)) == 3

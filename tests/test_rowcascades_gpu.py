@@ -147,3 +147,18 @@ def test_layer_norm(rf, level, n):
     ref = rc.layer_norm(x.numpy(), gamma.numpy(), beta.numpy(), 1e-5)
     # normalised values are O(1): relative bound plus a small absolute term
     assert np.all(np.abs(f64(y) - ref) <= 2e-3 * np.abs(ref) + 1e-4), np.abs(f64(y) - ref).max()
+
+
+@pytest.mark.parametrize("level", LEVELS)
+@pytest.mark.parametrize("n", [4, 1000, 4096, 8192])
+def test_rms_norm(rf, level, n):
+    g = torch.Generator().manual_seed(400 + n + level)
+    x = torch.randn(13, n, generator=g) * 3 - 1
+    x[5] = 0.0                                  # all-zero row: y = 0 (eps > 0)
+    gamma = torch.randn(n, generator=g)
+    y = torch.empty(13, n, device="cuda")
+    work = torch.empty(13, device="cuda") if level == 0 else None
+    rf.rf_rms_norm(x.cuda(), gamma.cuda(), 1e-6, y, level, work)
+    torch.cuda.synchronize()
+    ref = rc.rms_norm(x.numpy(), gamma.numpy(), 1e-6)
+    assert_close_f32(f64(y), ref, f"rms norm n={n} level={level}")

@@ -56,6 +56,23 @@ def test_fp32_single_row(rf):
     assert_close_f32(f64(out), ref, "fp32 out")
 
 
+@pytest.mark.parametrize("S", [1, 2, 4, 8])
+def test_fp32_short_rows_both_forms(rf, S):
+    # the short-sequence ablation's shape (512 keys, D = 64 fp32) on 64 rows:
+    # the incremental and non-incremental kernels both match the oracle
+    q, K, V = si.decode_inputs(64, 512, 64, torch.float32, seed=7)
+    scale = si.decode_scale(64)
+    ref, m, l = A.softmax_v_rows(f64(q), f64(K), f64(V), scale)
+    rm, rl, racc = A.segment_states(f64(q), f64(K), f64(V), scale, S)
+    out, lse, sm, sl, sa = run(rf, q, K, V, S, scale)
+    assert_close_f32(f64(out), ref, f"non-incremental out S={S}")
+    assert_states_close(f64(sm), f64(sl), f64(sa), rm, rl, racc, f"non-incremental states S={S}")
+    out2, lse2 = rf.attn_decode(q.cuda(), K.cuda(), V.cuda(), S, scale)
+    torch.cuda.synchronize()
+    assert_close_f32(f64(out2), ref, f"incremental out S={S}")
+    assert_close_f32(f64(lse2), m + np.log(l), f"incremental lse S={S}")
+
+
 def test_segments_longer_than_shared_memory_are_refused(rf):
     q, K, V = si.decode_inputs(1, 16385, 128, torch.bfloat16, seed=3)
     with pytest.raises(rf.RFError) as e:

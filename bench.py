@@ -303,7 +303,8 @@ def _events(torch, n):
 
 def time_graph(torch, calls, reps, warmup=3):
     """Capture ``calls`` (a list of zero-argument launchers) in one CUDA
-    graph; time ``reps`` replays; return ms per call."""
+    graph; time ``reps`` replays back to back (events between them); return
+    the median replay's ms per call."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -318,13 +319,16 @@ def time_graph(torch, calls, reps, warmup=3):
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
-    a, b = _events(torch, 2)
-    a.record()
-    for _ in range(reps):
+    # one event pair per replay; the median replay, per call
+    reps = max(reps, 5)
+    ev = _events(torch, reps + 1)
+    ev[0].record()
+    for i in range(reps):
         g.replay()
-    b.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / (reps * len(calls))
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+    return statistics.median(per) / len(calls)
 
 
 def roofline(bound, achieved, peak, unit, traffic):

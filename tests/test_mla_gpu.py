@@ -90,6 +90,11 @@ def test_head_groups(rf, H):
     check(rf, 2, H, 700, 3, si.mla_scale(), seed=90 + H)
 
 
+def test_head_groups_with_empty_segments(rf):
+    # several head groups (units dealt round-robin) and segments past the end
+    check(rf, 3, 64, 5, 8, si.mla_scale(), seed=94)
+
+
 def test_units_cross_sequences(rf):
     # 40 sequences x 8 segments = 320 units over the SMs: several units per
     # CTA, the query block reloaded where the sequence changes

@@ -227,16 +227,29 @@ rf_status launch_decode_split(const void* q, const void* k, const void* v, int R
   const int seg_len = (L + S - 1) / S;
   const float sl2 = scale * kLog2e;
   const unsigned grid = (unsigned)R * (unsigned)S;
-  constexpr int WARPS = 8, U = 8;
+  constexpr int WARPS = 8;
   const auto* qb = static_cast<const uint8_t*>(q);
   const auto* kb = static_cast<const uint8_t*>(k);
   const auto* vb = static_cast<const uint8_t*>(v);
+  // Segments of at most 128 keys: a shallower unroll (fewer loads in flight
+  // per warp, 40-44 registers instead of 98-104) lets an SM hold more CTAs,
+  // which is what keeps memory busy when every CTA's stream is short
+  // (measured: equal at 128 keys, 25 % faster at 64, slower from 256 up).
+  const bool short_seg = seg_len <= 128;
   if (dtype == RF_BF16 && D == 128) {
-    decode_split_kernel<Bf16Tag, WARPS, U><<<grid, WARPS * 32, 0, st>>>(
-        qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+    if (short_seg)
+      decode_split_kernel<Bf16Tag, WARPS, 2><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+    else
+      decode_split_kernel<Bf16Tag, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
   } else if (dtype == RF_F32 && D == 64) {
-    decode_split_kernel<float, WARPS, U><<<grid, WARPS * 32, 0, st>>>(
-        qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+    if (short_seg)
+      decode_split_kernel<float, WARPS, 2><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+    else
+      decode_split_kernel<float, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
   } else {
     return RF_ERR_UNSUPPORTED;
   }

@@ -231,21 +231,23 @@ rf_status launch_decode_split(const void* q, const void* k, const void* v, int R
   const auto* qb = static_cast<const uint8_t*>(q);
   const auto* kb = static_cast<const uint8_t*>(k);
   const auto* vb = static_cast<const uint8_t*>(v);
-  // Segments of at most 128 keys: a shallower unroll (fewer loads in flight
-  // per warp, 40-44 registers instead of 98-104) lets an SM hold more CTAs,
-  // which is what keeps memory busy when every CTA's stream is short
-  // (measured: equal at 128 keys, 25 % faster at 64, slower from 256 up).
-  const bool short_seg = seg_len <= 128;
+  // Segments of at most 128 keys: a shallower unroll (4 key pairs in flight
+  // per half-warp instead of 8, far fewer registers) lets an SM hold more
+  // CTAs, which is what keeps memory busy when every CTA's stream is short
+  // (measured on 512-key rows, D = 64: 5 % faster at 128 keys per segment,
+  // 28 % at 64; slower from 256 keys up).  With few CTAs in all (a single
+  // row) the deeper unroll keeps more in flight and stays faster.
+  const bool short_seg = seg_len <= 128 && grid >= 1024;   // many CTAs: occupancy decides
   if (dtype == RF_BF16 && D == 128) {
     if (short_seg)
-      decode_split_kernel<Bf16Tag, WARPS, 2><<<grid, WARPS * 32, 0, st>>>(
+      decode_split_kernel<Bf16Tag, WARPS, 4><<<grid, WARPS * 32, 0, st>>>(
           qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
     else
       decode_split_kernel<Bf16Tag, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(
           qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
   } else if (dtype == RF_F32 && D == 64) {
     if (short_seg)
-      decode_split_kernel<float, WARPS, 2><<<grid, WARPS * 32, 0, st>>>(
+      decode_split_kernel<float, WARPS, 4><<<grid, WARPS * 32, 0, st>>>(
           qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
     else
       decode_split_kernel<float, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(

@@ -14,7 +14,8 @@
 //     whole key rows (512 contiguous bytes), lane half h = lane/16 takes key
 //     2u+h of the tile and lane c = lane%16 the c-th 16-byte chunk of it;
 //   * K and V of a tile are loaded together (2*U 16-byte streaming loads per
-//     lane in flight), the partial dot products are summed across the 16
+//     lane in flight; U = 8, or 4 for short segments on large grids, where
+//     more CTAs per SM matter more), the partial dot products are summed across the 16
 //     lanes of a half with xor shuffles, so every lane of the half holds all
 //     U scores of its keys;
 //   * each half-warp keeps its own running state in the log2 domain

@@ -11,7 +11,10 @@ The convenience wrappers (``attn_decode``, ``softmax_topk``,
 with torch and call the entry points.
 
 There is no fallback: importing this package fails if librf.so has not been
-built (``cascaded_reductions_gb300._build.build()``).
+built (``cascaded_reductions_gb300._build.build()``).  The environment
+variable ``RF_LIBRARY`` names another build of the same library to load
+instead, e.g. the bounds-checked debug variant that
+``cascaded_reductions_gb300._build.build_checked()`` makes.
 """
 
 import ctypes
@@ -20,9 +23,10 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "librf.so")
+LIB_PATH = os.environ.get("RF_LIBRARY") or os.path.join(_HERE, "librf.so")
 
-RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_MISALIGNED, RF_ERR_CUDA, RF_ERR_TIMEOUT = range(6)
+(RF_OK, RF_ERR_INVALID_ARG, RF_ERR_UNSUPPORTED, RF_ERR_MISALIGNED, RF_ERR_CUDA, RF_ERR_TIMEOUT,
+ RF_ERR_BOUNDS) = range(7)
 RF_F32, RF_BF16 = 0, 1
 RF_FUSE_NONE, RF_FUSE_THREAD, RF_FUSE_WARP, RF_FUSE_BLOCK = range(4)
 
@@ -51,6 +55,8 @@ _SIGNATURES = {
     "rf_mla_decode_split": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_P, _P]),
     "rf_rms_norm": (_I, [_P, _P, _I, _I, _F, _P, _I, _P, _P]),
+    "rf_bounds_checked": (_I, []),
+    "rf_selftest_bounds": (_I, [_P]),
 }
 
 
@@ -333,8 +339,20 @@ def rf_selftest_wait_timeout(waited_ms, stream=None):
     _check(_lib.rf_selftest_wait_timeout(_ptr(waited_ms), _stream(stream)), "rf_selftest_wait_timeout")
 
 
+def rf_selftest_bounds(stream=None):
+    """One refused index through the bounds check (bounds-checked build only);
+    RF_ERR_BOUNDS then shows up in rf_device_error()."""
+    _check(_lib.rf_selftest_bounds(_stream(stream)), "rf_selftest_bounds")
+
+
+def rf_bounds_checked():
+    """True if the loaded library checks every kernel's global indices."""
+    return bool(_lib.rf_bounds_checked())
+
+
 def rf_device_error(stream=None):
-    """Synchronise and return (and clear) the bounded-wait status word."""
+    """Synchronise and return (and clear) the on-device status words: bounded
+    waits, and in the bounds-checked build the index checks."""
     st = _I(0)
     _check(_lib.rf_device_error(ctypes.byref(st), _stream(stream)), "rf_device_error")
     return st.value

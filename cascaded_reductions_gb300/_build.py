@@ -57,15 +57,21 @@ def _compile(nvcc, src, obj, extra):
     return r.stderr
 
 
-def build(force=False, verbose=False, extra_flags=()):
-    """Compile every CUDA source and link librf.so; returns the library path."""
+def build(force=False, verbose=False, extra_flags=(), lib=None, objdir=None):
+    """Compile every CUDA source and link librf.so; returns the library path.
+
+    ``lib`` / ``objdir`` build a variant elsewhere (e.g. the bounds-checked
+    debug library, ``extra_flags=["-DRF_CHECK_BOUNDS"]``) without touching
+    the default one."""
+    lib = lib or LIB
+    objdir = objdir or OBJDIR
     srcs = _sources()
     hdrs = _headers()
-    if not force and not _stale(LIB, srcs + hdrs):
-        return LIB
+    if not force and not _stale(lib, srcs + hdrs):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(OBJDIR, exist_ok=True)
-    objs = [os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    os.makedirs(objdir, exist_ok=True)
+    objs = [os.path.join(objdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
     jobs = []
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         for s, o in zip(srcs, objs):
@@ -76,13 +82,20 @@ def build(force=False, verbose=False, extra_flags=()):
         for lg in logs:
             if lg:
                 print(lg)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of librf.so failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_checked(force=False):
+    """The bounds-checked debug variant: _build_checked/librf_checked.so."""
+    d = os.path.join(HERE, "_build_checked")
+    return build(force=force, extra_flags=["-DRF_CHECK_BOUNDS"],
+                 lib=os.path.join(d, "librf_checked.so"), objdir=d)
 
 
 if __name__ == "__main__":

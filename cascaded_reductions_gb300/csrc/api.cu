@@ -21,6 +21,7 @@ const char* rf_status_string(int status) {
     case RF_ERR_MISALIGNED: return "RF_ERR_MISALIGNED";
     case RF_ERR_CUDA: return "RF_ERR_CUDA";
     case RF_ERR_TIMEOUT: return "RF_ERR_TIMEOUT";
+    case RF_ERR_BOUNDS: return "RF_ERR_BOUNDS";
     default: return "RF_ERR_UNKNOWN";
   }
 }
@@ -218,4 +219,21 @@ rf_status rf_device_error(int* status, void* stream) {
 rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream) {
   if (!waited_ms) return RF_ERR_INVALID_ARG;
   return rf::launch_selftest_wait_timeout(waited_ms, as_stream(stream));
+}
+
+int rf_bounds_checked(void) {
+#ifdef RF_CHECK_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+rf_status rf_selftest_bounds(void* stream) {
+#ifdef RF_CHECK_BOUNDS
+  return rf::launch_selftest_bounds(as_stream(stream));
+#else
+  (void)stream;
+  return RF_ERR_UNSUPPORTED;
+#endif
 }

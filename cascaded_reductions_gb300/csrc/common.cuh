@@ -81,6 +81,48 @@ struct Chunk<Bf16Tag> {
 // exp2(x - ref) is then 0 for x = -inf and the state stays the identity.
 __device__ __forceinline__ float ref_of(float m) { return m == -INFINITY ? 0.f : m; }
 
+// ------------------------------------------------------- bounds checks ----
+// Built with -DRF_CHECK_BOUNDS, every kernel checks each global load and
+// store against the extent of its buffer, computed in the kernel from the
+// call's size arguments (never from the pointer it is checking).  A refused
+// index skips its access (a load yields zeros) and records RF_ERR_BOUNDS in
+// this translation unit's device word; rf_device_error reads and clears the
+// words of every file through the functions registered with
+// register_bounds_word.  Without the flag RF_SPAN_OK is the constant true and
+// the checks compile to nothing.
+#ifdef RF_CHECK_BOUNDS
+static __device__ int g_bounds_status;
+// elements [i, i + w) of a buffer of n elements
+__device__ __forceinline__ bool span_ok(long long i, long long w, long long n) {
+  if (i >= 0 && i + w <= n) return true;
+  atomicExch(&g_bounds_status, (int)RF_ERR_BOUNDS);
+  return false;
+}
+#define RF_SPAN_OK(i, w, n) ::rf::span_ok((long long)(i), (long long)(w), (long long)(n))
+using bounds_take_fn = rf_status (*)(int*);
+bool register_bounds_word(bounds_take_fn take);
+#define RF_BOUNDS_WORD_OF_THIS_FILE                                                       \
+  namespace {                                                                             \
+  rf_status take_bounds_word(int* status) {                                               \
+    int v = 0, zero = 0;                                                                  \
+    if (cudaMemcpyFromSymbol(&v, g_bounds_status, sizeof(int)) != cudaSuccess)           \
+      return RF_ERR_CUDA;                                                                 \
+    if (cudaMemcpyToSymbol(g_bounds_status, &zero, sizeof(int)) != cudaSuccess)          \
+      return RF_ERR_CUDA;                                                                 \
+    *status = v;                                                                          \
+    return RF_OK;                                                                         \
+  }                                                                                       \
+  const bool g_bounds_word_registered = register_bounds_word(&take_bounds_word);          \
+  }
+#else
+#define RF_SPAN_OK(i, w, n) true
+#define RF_BOUNDS_WORD_OF_THIS_FILE
+#endif
+#define RF_IDX_OK(i, n) RF_SPAN_OK(i, 1, n)
+// read-all-bounds-words half of rf_device_error (RF_OK with *status = 0 when
+// the build has no checks)
+rf_status take_bounds_words(int* status);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Opt a kernel into `bytes` of dynamic shared memory on the current device,
@@ -140,6 +182,7 @@ rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, i
 rf_status mla_take_status(int* status);
 rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st);
 rf_status selftest_take_status(int* status);
+rf_status launch_selftest_bounds(cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);
 // read and clear the bounded-wait status word of each tensor-core kernel file
 rf_status gemm_take_status(int* status);

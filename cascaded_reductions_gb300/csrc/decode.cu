@@ -52,9 +52,12 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
   const int a = min(L, seg * seg_len);
   const int b = min(L, a + seg_len);
 
-  // this lane's chunk of q, pre-scaled into the log2 domain
+  // this lane's chunk of q, pre-scaled into the log2 domain (R = gridDim.x / S rows)
   float qf[E];
-  Chunk<T>::unpack(*reinterpret_cast<const uint4*>(q + (size_t)row * ROW_BYTES + c * 16), qf);
+  uint4 qv = make_uint4(0, 0, 0, 0);
+  if (RF_SPAN_OK((size_t)row * ROW_BYTES + c * 16, 16, (long long)(gridDim.x / S) * ROW_BYTES))
+    qv = *reinterpret_cast<const uint4*>(q + (size_t)row * ROW_BYTES + c * 16);
+  Chunk<T>::unpack(qv, qf);
 #pragma unroll
   for (int e = 0; e < E; ++e) qf[e] *= scale_log2;
 
@@ -71,7 +74,8 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = t0 + 2 * u + half;
-      if (key < b) {
+      if (key < b && RF_SPAN_OK(((size_t)row * L + key) * ROW_BYTES + c * 16, 16,
+                                (long long)(gridDim.x / S) * L * ROW_BYTES)) {
         kv[u] = ld_stream_v4(kr + (size_t)key * ROW_BYTES);
         vv[u] = ld_stream_v4(vr + (size_t)key * ROW_BYTES);
       } else {
@@ -156,8 +160,8 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
       A = fmaf(f, sm_acc[w][d], A);
       Lsum = fmaf(f, sm_l[w], Lsum);
     }
-    seg_acc[state * D + d] = A;
-    if (d == 0) {
+    if (RF_IDX_OK(state * D + d, (long long)gridDim.x * D)) seg_acc[state * D + d] = A;
+    if (d == 0 && RF_IDX_OK(state, gridDim.x)) {
       seg_m[state] = M * kLn2;   // -inf stays -inf
       seg_l[state] = Lsum;
     }
@@ -185,12 +189,14 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
   const float* lr = seg_l + (size_t)row * S;
 
   float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) M = fmaxf(M, mr[s]);
+  for (int s = lane; s < S; s += 32)
+    if (RF_IDX_OK((size_t)row * S + s, (long long)R * S)) M = fmaxf(M, mr[s]);
   M = group_max<32>(M);
   const float ref = M == -INFINITY ? 0.f : M;
 
   float Lsum = 0.f;
-  for (int s = lane; s < S; s += 32) Lsum = fmaf(expf(mr[s] - ref), lr[s], Lsum);
+  for (int s = lane; s < S; s += 32)
+    if (RF_IDX_OK((size_t)row * S + s, (long long)R * S)) Lsum = fmaf(expf(mr[s] - ref), lr[s], Lsum);
   Lsum = group_sum<32>(Lsum);
 
   if (lane < LANES) {
@@ -198,6 +204,7 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
     const float4* ar =
         reinterpret_cast<const float4*>(seg_acc + (size_t)row * S * D) + part * 32 + lane;
     for (int s = 0; s < S; ++s) {
+      if (!RF_IDX_OK(((size_t)row * S + s) * V4 + part * 32 + lane, (long long)R * S * V4)) continue;
       const float f = expf(mr[s] - ref);
       const float4 x = ar[(size_t)s * V4];
       A.x = fmaf(f, x.x, A.x);
@@ -208,7 +215,8 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
     const float inv = 1.f / Lsum;
     A.x *= inv; A.y *= inv; A.z *= inv; A.w *= inv;
     const size_t o = (size_t)row * V4 + part * 32 + lane;
-    if (BF16_OUT) {
+    if (!RF_IDX_OK(o, (long long)R * V4)) {
+    } else if (BF16_OUT) {
       uint2 p;
       p.x = pack_bf16x2(A.x, A.y);
       p.y = pack_bf16x2(A.z, A.w);
@@ -217,7 +225,7 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
       reinterpret_cast<float4*>(out)[o] = A;
     }
   }
-  if (lse != nullptr && lane == 0 && part == 0) lse[row] = M + logf(Lsum);
+  if (lse != nullptr && lane == 0 && part == 0 && RF_IDX_OK(row, R)) lse[row] = M + logf(Lsum);
 }
 
 }  // namespace
@@ -278,5 +286,7 @@ rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float
   }
   return launch_status();
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

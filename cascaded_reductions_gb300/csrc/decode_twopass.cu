@@ -52,7 +52,10 @@ decode_twopass_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
   const int b = min(L, a + seg_len);
 
   float qf[E];
-  Chunk<T>::unpack(*reinterpret_cast<const uint4*>(q + (size_t)row * ROW_BYTES + c * 16), qf);
+  uint4 qv = make_uint4(0, 0, 0, 0);
+  if (RF_SPAN_OK((size_t)row * ROW_BYTES + c * 16, 16, (long long)(gridDim.x / S) * ROW_BYTES))
+    qv = *reinterpret_cast<const uint4*>(q + (size_t)row * ROW_BYTES + c * 16);
+  Chunk<T>::unpack(qv, qf);
 #pragma unroll
   for (int e = 0; e < E; ++e) qf[e] *= scale_log2;
   const uint8_t* kr = k + (size_t)row * L * ROW_BYTES + c * 16;
@@ -65,7 +68,10 @@ decode_twopass_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = t0 + 2 * u + half;
-      kv[u] = key < b ? ld_stream_v4(kr + (size_t)key * ROW_BYTES) : make_uint4(0, 0, 0, 0);
+      kv[u] = key < b && RF_SPAN_OK(((size_t)row * L + key) * ROW_BYTES + c * 16, 16,
+                                    (long long)(gridDim.x / S) * L * ROW_BYTES)
+                  ? ld_stream_v4(kr + (size_t)key * ROW_BYTES)
+                  : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -77,7 +83,7 @@ decode_twopass_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
       d = group_sum<16>(d);
       const int key = t0 + 2 * u + half;
       if (key < b) {
-        if (c == 0) sc[key - a] = d;
+        if (c == 0 && RF_IDX_OK(key - a, seg_len)) sc[key - a] = d;   // seg_len floats of smem
         mloc = fmaxf(mloc, d);
       }
     }
@@ -100,12 +106,15 @@ decode_twopass_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = t0 + 2 * u + half;
-      vv[u] = key < b ? ld_stream_v4(vr + (size_t)key * ROW_BYTES) : make_uint4(0, 0, 0, 0);
+      vv[u] = key < b && RF_SPAN_OK(((size_t)row * L + key) * ROW_BYTES + c * 16, 16,
+                                    (long long)(gridDim.x / S) * L * ROW_BYTES)
+                  ? ld_stream_v4(vr + (size_t)key * ROW_BYTES)
+                  : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int key = t0 + 2 * u + half;
-      const float p = key < b ? exp2f(sc[key - a] - ref) : 0.f;
+      const float p = key < b && RF_IDX_OK(key - a, seg_len) ? exp2f(sc[key - a] - ref) : 0.f;
       l += p;
       float vf[E];
       Chunk<T>::unpack(vv[u], vf);
@@ -128,8 +137,8 @@ decode_twopass_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__
     float A = 0.f;
 #pragma unroll
     for (int w = 0; w < WARPS; ++w) A += sm_acc[w][d];
-    seg_acc[state * D + d] = A;
-    if (d == 0) {
+    if (RF_IDX_OK(state * D + d, (long long)gridDim.x * D)) seg_acc[state * D + d] = A;
+    if (d == 0 && RF_IDX_OK(state, gridDim.x)) {
       float Ls = 0.f;
 #pragma unroll
       for (int w = 0; w < WARPS; ++w) Ls += sm_l[w];
@@ -170,5 +179,7 @@ rf_status launch_decode_twopass(const void* q, const void* k, const void* v, int
     return launch_twopass_t<float>(q, k, v, R, L, S, seg_len, sl2, seg_m, seg_l, seg_acc, st);
   return RF_ERR_UNSUPPORTED;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

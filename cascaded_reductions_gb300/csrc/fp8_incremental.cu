@@ -252,28 +252,29 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
     if (ok && tc::mbar_wait(&sh->acc_done, (uint32_t)(T - 1) & 1u, abort)) {
       tc::fence_after_sync();
       const int row = m0 + r;
-      __nv_bfloat16* yrow = y + (size_t)row * N + n0 + half * 256;
-      const float4* swv = reinterpret_cast<const float4*>(sw + n0 + half * 256);
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
         tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(half * 256 + c * 32), v);
         tc::tmem_ld_wait();
+        const int col0 = n0 + half * 256 + c * 32;
+        if (!RF_SPAN_OK(col0, 32, N) || !RF_SPAN_OK((size_t)row * N + col0, 32, (long long)M * N))
+          continue;                            // (checked build) sw and y spans
         uint32_t p[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float4 s4 = __ldg(swv + c * 8 + j);
+          const float4 s4 = __ldg(reinterpret_cast<const float4*>(sw + col0) + j);
           p[2 * j] = pack_bf16x2(__uint_as_float(v[4 * j]) * s_cur * s4.x,
                                  __uint_as_float(v[4 * j + 1]) * s_cur * s4.y);
           p[2 * j + 1] = pack_bf16x2(__uint_as_float(v[4 * j + 2]) * s_cur * s4.z,
                                      __uint_as_float(v[4 * j + 3]) * s_cur * s4.w);
         }
-        uint4* dst = reinterpret_cast<uint4*>(yrow + c * 32);
+        uint4* dst = reinterpret_cast<uint4*>(y + (size_t)row * N + col0);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
       }
-      if (half == 0 && n0 == 0 && sx_out != nullptr) sx_out[row] = s_cur;
+      if (half == 0 && n0 == 0 && sx_out != nullptr && RF_IDX_OK(row, M)) sx_out[row] = s_cur;
     }
   }
 
@@ -310,5 +311,7 @@ rf_status fp8_incremental_take_status(int* status) {
   *status = v;
   return RF_OK;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

@@ -181,7 +181,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
       item(i, tm, tcol0, width);
       const int row = tm * BM + r;
       const bool row_in = row < M;
-      const float srow = row_in ? sx[row] : 0.f;
+      const float srow = row_in && RF_IDX_OK(row, M) ? sx[row] : 0.f;
       __nv_bfloat16* yrow = y + (size_t)(row_in ? row : 0) * N;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
 #pragma unroll 1
@@ -193,6 +193,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (!row_in || col0 >= N) continue;
         if (col0 + 32 <= N && (N & 7) == 0) {
           // whole 32-column chunk, 16-byte aligned row: vector loads and stores
+          if (!RF_SPAN_OK(col0, 32, N) || !RF_SPAN_OK((size_t)row * N + col0, 32, (long long)M * N))
+            continue;                          // (checked build) sw and y spans
           const float4* swv = reinterpret_cast<const float4*>(sw + col0);
           uint32_t p[16];
 #pragma unroll
@@ -212,7 +214,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int col = col0 + j;
-            if (col < N)
+            if (col < N && RF_IDX_OK((size_t)row * N + col, (long long)M * N))
               yrow[col] = __float2bfloat16_rn(__uint_as_float(v[j]) * srow * __ldg(sw + col));
           }
         }
@@ -271,5 +273,7 @@ rf_status gemm_take_status(int* status) {
   *status = v;
   return RF_OK;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

@@ -346,9 +346,11 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
       const size_t st0 = ((size_t)x.b * H + (size_t)x.g * HG) * S + x.s;   // state of head 0
       if (x.nt == 0) {
         // empty segment: the identity state
+        // (checked build) states: units * HG = B * H * S of them
         for (int i = threadIdx.x - 64; i < HG * DV; i += THREADS - 64)
-          seg_acc[(st0 + (size_t)(i / DV) * S) * DV + (i % DV)] = 0.f;
-        if (quarter == 0 && lane < HW) {
+          if (RF_IDX_OK((st0 + (size_t)(i / DV) * S) * DV + (i % DV), units * HG * DV))
+            seg_acc[(st0 + (size_t)(i / DV) * S) * DV + (i % DV)] = 0.f;
+        if (quarter == 0 && lane < HW && RF_IDX_OK(st0 + (size_t)(hb + lane) * S, units * HG)) {
           seg_m[st0 + (size_t)(hb + lane) * S] = -INFINITY;
           seg_l[st0 + (size_t)(hb + lane) * S] = 0.f;
         }
@@ -459,8 +461,10 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           }
         const int hd = hb + lane;
         const float lt = (sh->lred[0][hd] + sh->lred[1][hd]) + (sh->lred[2][hd] + sh->lred[3][hd]);
-        seg_l[st0 + (size_t)hd * S] = lt * fk;
-        seg_m[st0 + (size_t)hd * S] = mk * kLn2;
+        if (RF_IDX_OK(st0 + (size_t)hd * S, units * HG)) {
+          seg_l[st0 + (size_t)hd * S] = lt * fk;
+          seg_m[st0 + (size_t)hd * S] = mk * kLn2;
+        }
       }
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -469,7 +473,9 @@ mla_decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         tc::tmem_ld_wait();
         float* dst = seg_acc + (st0 + (size_t)hb * S) * DV + c * BK + kt;
 #pragma unroll
-        for (int h = 0; h < HW; ++h) dst[(size_t)h * S * DV] = __uint_as_float(r[h]) * f[h];
+        for (int h = 0; h < HW; ++h)
+          if (RF_IDX_OK((st0 + (size_t)(hb + h) * S) * DV + c * BK + kt, units * HG * DV))
+            dst[(size_t)h * S * DV] = __uint_as_float(r[h]) * f[h];
       }
       tc::fence_before_sync();
     }
@@ -520,5 +526,7 @@ rf_status mla_take_status(int* status) {
   *status = v;
   return RF_OK;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

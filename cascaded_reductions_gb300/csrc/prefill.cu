@@ -404,13 +404,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * inv,
                                  __uint_as_float(v[2 * i + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-          if (row_in) {
+          // (checked build) 32 outputs inside out[B*H = gridDim.x / NP][N][HD]
+          if (row_in && RF_SPAN_OK((size_t)grow * HD + col0 + c * 32, 32,
+                                   (long long)(gridDim.x / NP) * N * HD)) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
           }
         }
-        if (lse != nullptr && half == 0 && row_in) lse[grow] = (m_ref + log2f(lt)) * kLn2;
+        if (lse != nullptr && half == 0 && row_in &&
+            RF_IDX_OK(grow, (long long)(gridDim.x / NP) * N))
+          lse[grow] = (m_ref + log2f(lt)) * kLn2;
       }
     }
   }
@@ -454,5 +458,7 @@ rf_status prefill_take_status(int* status) {
   *status = v;
   return RF_OK;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

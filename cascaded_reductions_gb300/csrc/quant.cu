@@ -68,26 +68,26 @@ absmax_quant_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict__ xq,
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * THREADS + threadIdx.x;
-    if (c < K8) {
+    if (c < K8 && RF_IDX_OK(base + c, (long long)gridDim.x * K8)) {   // M = gridDim.x rows of K8 chunks
       v[i] = ld_stream_v4(x + base + c);
       a = absmax8(v[i], a);
     }
   }
   const float amax = block_max<THREADS>(absmax_value(a), red);
   const float s = __fdiv_rn(amax, 448.f);
-  if (threadIdx.x == 0) sx[blockIdx.x] = s;
+  if (threadIdx.x == 0 && RF_IDX_OK(blockIdx.x, gridDim.x)) sx[blockIdx.x] = s;
   if (fast_scale(s)) {
     const float r = __frcp_rn(s);
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int c = i * THREADS + threadIdx.x;
-      if (c < K8) xq[base + c] = encode8(v[i], s, r);
+      if (c < K8 && RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8(v[i], s, r);
     }
   } else {
 #pragma unroll 1
     for (int i = 0; i < VPT; ++i) {
       const int c = i * THREADS + threadIdx.x;
-      if (c < K8) xq[base + c] = encode8_exact(v[i], s);
+      if (c < K8 && RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8_exact(v[i], s);
     }
   }
 }
@@ -100,15 +100,18 @@ absmax_quant_long_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict_
   __shared__ float red[THREADS / 32];
   const size_t base = (size_t)blockIdx.x * K8;
   uint32_t a = 0u;
-  for (int c = threadIdx.x; c < K8; c += THREADS) a = absmax8(x[base + c], a);
+  for (int c = threadIdx.x; c < K8; c += THREADS)
+    if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) a = absmax8(x[base + c], a);
   const float amax = block_max<THREADS>(absmax_value(a), red);
   const float s = __fdiv_rn(amax, 448.f);
-  if (threadIdx.x == 0) sx[blockIdx.x] = s;
+  if (threadIdx.x == 0 && RF_IDX_OK(blockIdx.x, gridDim.x)) sx[blockIdx.x] = s;
   if (fast_scale(s)) {
     const float r = __frcp_rn(s);
-    for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8(x[base + c], s, r);
+    for (int c = threadIdx.x; c < K8; c += THREADS)
+      if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8(x[base + c], s, r);
   } else {
-    for (int c = threadIdx.x; c < K8; c += THREADS) xq[base + c] = encode8_exact(x[base + c], s);
+    for (int c = threadIdx.x; c < K8; c += THREADS)
+      if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8_exact(x[base + c], s);
   }
 }
 
@@ -135,5 +138,7 @@ rf_status launch_absmax_quant(const void* x, int M, int K, uint8_t* xq, float* s
 #undef RF_QUANT_CASE
   return launch_status();
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

@@ -86,6 +86,15 @@ __device__ __forceinline__ float bsum(float v, float* red) {
   return r;
 }
 
+// Bounds checks of the row accesses (no-ops unless built with RF_CHECK_BOUNDS):
+// float4 chunk c of this block's row in a buffer of gridDim.x rows of `width`
+// floats, and chunk c of a vector of n floats.  Outputs of one value per row
+// are indexed by blockIdx.x alone and need none.
+__device__ __forceinline__ bool row_ok(long long c, long long width) {
+  return RF_SPAN_OK((long long)blockIdx.x * width + 4 * c, 4, (long long)gridDim.x * width);
+}
+__device__ __forceinline__ bool vec_ok(long long c, long long n) { return RF_SPAN_OK(4 * c, 4, n); }
+
 __device__ __forceinline__ float get(const float4& v, int e) {
   return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
 }
@@ -103,7 +112,7 @@ softmax_fused_kernel(const float* __restrict__ x, int n, float* __restrict__ y) 
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    v[i] = c < n4 ? __ldcs(xr + c) : make_float4(NI, NI, NI, NI);
+    v[i] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(NI, NI, NI, NI);
   }
   SmState st{-INFINITY, 0.f};
   if (LEVEL == RF_FUSE_THREAD) {
@@ -158,7 +167,7 @@ softmax_fused_kernel(const float* __restrict__ x, int n, float* __restrict__ y) 
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    if (c < n4)
+    if (c < n4 && row_ok(c, n))
       __stcs(yr + c, make_float4(__expf(v[i].x - st.m) * inv, __expf(v[i].y - st.m) * inv,
                                  __expf(v[i].z - st.m) * inv, __expf(v[i].w - st.m) * inv));
   }
@@ -171,6 +180,7 @@ softmax_max_kernel(const float* __restrict__ x, int n, float* __restrict__ work)
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
   float m = -INFINITY;
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
   }
@@ -185,11 +195,12 @@ softmax_sum_kernel(const float* __restrict__ x, int n, int R, float* __restrict_
   const float m = work[blockIdx.x];
   float s = 0.f;
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     s += __expf(v.x - m) + __expf(v.y - m) + __expf(v.z - m) + __expf(v.w - m);
   }
   s = bsum(s, red);
-  if (threadIdx.x == 0) work[R + blockIdx.x] = s;
+  if (threadIdx.x == 0 && RF_IDX_OK(R + blockIdx.x, 2LL * gridDim.x)) work[R + blockIdx.x] = s;
 }
 
 __global__ void __launch_bounds__(TH)
@@ -199,6 +210,7 @@ softmax_norm_kernel(const float* __restrict__ x, int n, int R, const float* __re
   float4* yr = reinterpret_cast<float4*>(y + (size_t)blockIdx.x * n);
   const float m = work[blockIdx.x], inv = 1.f / work[R + blockIdx.x];
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     __stcs(yr + c, make_float4(__expf(v.x - m) * inv, __expf(v.y - m) * inv,
                                __expf(v.z - m) * inv, __expf(v.w - m) * inv));
@@ -247,7 +259,7 @@ variance_fused_kernel(const float* __restrict__ x, int n, float* __restrict__ me
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base + u * TH + (int)threadIdx.x;
-        v[u] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -274,7 +286,7 @@ variance_fused_kernel(const float* __restrict__ x, int n, float* __restrict__ me
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base0 + u * TH + lane;
-        v[u] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -300,7 +312,7 @@ variance_fused_kernel(const float* __restrict__ x, int n, float* __restrict__ me
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int c = base0 + u * TH + (int)threadIdx.x;
-        v[u] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -328,6 +340,7 @@ mean_kernel(const float* __restrict__ x, int n, float* __restrict__ mean_out) {
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
   float s = 0.f;
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     s += (v.x + v.y) + (v.z + v.w);
   }
@@ -343,6 +356,7 @@ var_from_mean_kernel(const float* __restrict__ x, int n, const float* __restrict
   const float mu = mean_in[blockIdx.x];
   float s = 0.f;
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     const float dx = v.x - mu, dy = v.y - mu, dz = v.z - mu, dw = v.w - mu;
     s += (dx * dx + dy * dy) + (dz * dz + dw * dw);
@@ -414,10 +428,10 @@ inertia_fused_kernel(const float* __restrict__ mass, const float* __restrict__ p
       for (int u = 0; u < 2; ++u) {
         const int c = base + u * TH + (int)threadIdx.x;
         const bool ok = c < n4;
-        mv[u] = ok ? __ldcs(mr + c) : zero;
-        xv[u] = ok ? __ldcs(xr + c) : zero;
-        yv[u] = ok ? __ldcs(yr + c) : zero;
-        zv[u] = ok ? __ldcs(zr + c) : zero;
+        mv[u] = ok && row_ok(c, n) ? __ldcs(mr + c) : zero;
+        xv[u] = ok && row_ok(c, 3LL * n) ? __ldcs(xr + c) : zero;
+        yv[u] = ok && row_ok(n4 + c, 3LL * n) ? __ldcs(yr + c) : zero;
+        zv[u] = ok && row_ok(2 * n4 + c, 3LL * n) ? __ldcs(zr + c) : zero;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -450,10 +464,10 @@ inertia_fused_kernel(const float* __restrict__ mass, const float* __restrict__ p
       for (int u = 0; u < 2; ++u) {
         const int c = base0 + u * TH + lane;
         const bool ok = c < n4;
-        mv[u] = ok ? __ldcs(mr + c) : zero;
-        xv[u] = ok ? __ldcs(xr + c) : zero;
-        yv[u] = ok ? __ldcs(yr + c) : zero;
-        zv[u] = ok ? __ldcs(zr + c) : zero;
+        mv[u] = ok && row_ok(c, n) ? __ldcs(mr + c) : zero;
+        xv[u] = ok && row_ok(c, 3LL * n) ? __ldcs(xr + c) : zero;
+        yv[u] = ok && row_ok(n4 + c, 3LL * n) ? __ldcs(yr + c) : zero;
+        zv[u] = ok && row_ok(2 * n4 + c, 3LL * n) ? __ldcs(zr + c) : zero;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -472,10 +486,10 @@ inertia_fused_kernel(const float* __restrict__ mass, const float* __restrict__ p
       for (int u = 0; u < 2; ++u) {
         const int c = base0 + u * TH + (int)threadIdx.x;
         const bool ok = c < n4;
-        mv[u] = ok ? __ldcs(mr + c) : zero;
-        xv[u] = ok ? __ldcs(xr + c) : zero;
-        yv[u] = ok ? __ldcs(yr + c) : zero;
-        zv[u] = ok ? __ldcs(zr + c) : zero;
+        mv[u] = ok && row_ok(c, n) ? __ldcs(mr + c) : zero;
+        xv[u] = ok && row_ok(c, 3LL * n) ? __ldcs(xr + c) : zero;
+        yv[u] = ok && row_ok(n4 + c, 3LL * n) ? __ldcs(yr + c) : zero;
+        zv[u] = ok && row_ok(2 * n4 + c, 3LL * n) ? __ldcs(zr + c) : zero;
       }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -502,6 +516,7 @@ center_kernel(const float* __restrict__ mass, const float* __restrict__ pos, int
   const float4* xr = reinterpret_cast<const float4*>(pos + (size_t)blockIdx.x * 3 * n);
   float M = 0.f, sx = 0.f, sy = 0.f, sz = 0.f;
   for (int c = threadIdx.x; c < n4; c += TH) {
+    if (!row_ok(c, n) || !row_ok(2 * n4 + c, 3LL * n)) continue;
     const float4 m = __ldcs(mr + c), px = __ldcs(xr + c), py = __ldcs(xr + n4 + c),
                  pz = __ldcs(xr + 2 * n4 + c);
     M += (m.x + m.y) + (m.z + m.w);
@@ -531,6 +546,7 @@ inertia_from_center_kernel(const float* __restrict__ mass, const float* __restri
               cz = center[blockIdx.x * 3 + 2];
   float I = 0.f;
   for (int c = threadIdx.x; c < n4; c += TH) {
+    if (!row_ok(c, n) || !row_ok(2 * n4 + c, 3LL * n)) continue;
     const float4 m = __ldcs(mr + c), px = __ldcs(xr + c), py = __ldcs(xr + n4 + c),
                  pz = __ldcs(xr + 2 * n4 + c);
 #pragma unroll
@@ -560,7 +576,7 @@ layernorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ ga
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    v[i] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[i] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (c < n4) {
       cnt += 4.f;
       sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
@@ -587,7 +603,7 @@ layernorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ ga
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    if (c < n4) {
+    if (c < n4 && row_ok(c, n) && vec_ok(c, n)) {
       const float4 g = __ldg(g4 + c), b = __ldg(b4 + c);
       __stcs(yr + c, make_float4((v[i].x - mu) * rstd * g.x + b.x, (v[i].y - mu) * rstd * g.y + b.y,
                                  (v[i].z - mu) * rstd * g.z + b.z, (v[i].w - mu) * rstd * g.w + b.w));
@@ -606,6 +622,7 @@ layernorm_apply_kernel(const float* __restrict__ x, const float* __restrict__ ga
   const float4* g4 = reinterpret_cast<const float4*>(gamma);
   const float4* b4 = reinterpret_cast<const float4*>(beta);
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n) || !vec_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c), g = __ldg(g4 + c), b = __ldg(b4 + c);
     __stcs(yr + c, make_float4((v.x - mu) * rstd * g.x + b.x, (v.y - mu) * rstd * g.y + b.y,
                                (v.z - mu) * rstd * g.z + b.z, (v.w - mu) * rstd * g.w + b.w));
@@ -629,7 +646,7 @@ rmsnorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ gamm
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    v[i] = c < n4 ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[i] = c < n4 && row_ok(c, n) ? __ldcs(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     ss += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
   }
   const float rs = rsqrtf(bsum(ss, red) / (float)n + eps);
@@ -637,7 +654,7 @@ rmsnorm_fused_kernel(const float* __restrict__ x, const float* __restrict__ gamm
 #pragma unroll
   for (int i = 0; i < VPT; ++i) {
     const int c = i * TH + threadIdx.x;
-    if (c < n4) {
+    if (c < n4 && row_ok(c, n) && vec_ok(c, n)) {
       const float4 g = __ldg(g4 + c);
       __stcs(yr + c, make_float4(v[i].x * rs * g.x, v[i].y * rs * g.y, v[i].z * rs * g.z,
                                  v[i].w * rs * g.w));
@@ -652,6 +669,7 @@ meansq_kernel(const float* __restrict__ x, int n, float* __restrict__ ms_out) {
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)blockIdx.x * n);
   float s = 0.f;
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c);
     s += (v.x * v.x + v.y * v.y) + (v.z * v.z + v.w * v.w);
   }
@@ -667,6 +685,7 @@ rmsnorm_apply_kernel(const float* __restrict__ x, const float* __restrict__ gamm
   const float rs = rsqrtf(ms[blockIdx.x] + eps);
   const float4* g4 = reinterpret_cast<const float4*>(gamma);
   for (int c = threadIdx.x; c < (n >> 2); c += TH) {
+    if (!row_ok(c, n) || !vec_ok(c, n)) continue;
     const float4 v = __ldcs(xr + c), g = __ldg(g4 + c);
     __stcs(yr + c, make_float4(v.x * rs * g.x, v.y * rs * g.y, v.z * rs * g.z, v.w * rs * g.w));
   }
@@ -762,5 +781,7 @@ rf_status launch_moment_of_inertia(const float* mass, const float* pos, int R, i
   }
   return launch_status();
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

@@ -1,4 +1,5 @@
-// Self-test of the bounded waits the tensor-core kernels use.
+// Self-tests of the on-device checks: the bounded waits the tensor-core
+// kernels use, and (bounds-checked build) the index checks of every kernel.
 //
 // One thread waits on a shared-memory mbarrier that nothing ever arrives on,
 // through the same tc::mbar_wait every pipeline wait in this library uses.
@@ -29,7 +30,26 @@ __global__ void wait_timeout_kernel(int* __restrict__ waited_ms) {
   }
 }
 
+#ifdef RF_CHECK_BOUNDS
+__device__ int g_selftest_sink[1];
+
+// Presents the index n to the check of an n-element buffer: one past the
+// end, so the check refuses it and records RF_ERR_BOUNDS.  The store it
+// guards targets element 0, a valid address, so nothing faults even if the
+// check were wrong.
+__global__ void bounds_selftest_kernel(int n) {
+  if (RF_IDX_OK(n, n)) g_selftest_sink[0] = 1;
+}
+#endif
+
 }  // namespace
+
+#ifdef RF_CHECK_BOUNDS
+rf_status launch_selftest_bounds(cudaStream_t st) {
+  bounds_selftest_kernel<<<1, 1, 0, st>>>(1);
+  return launch_status();
+}
+#endif
 
 rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st) {
   wait_timeout_kernel<<<1, 32, 0, st>>>(waited_ms);
@@ -43,5 +63,7 @@ rf_status selftest_take_status(int* status) {
   *status = v;
   return RF_OK;
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

@@ -97,7 +97,7 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k_rt, in
 #pragma unroll
     for (int c = 0; c < NV / W; ++c) {
       const int e0 = c * G * W + gl * W;
-      const bool in = live && e0 < E;
+      const bool in = live && e0 < E && RF_SPAN_OK(e0, W, E) && RF_IDX_OK(token, T);
       if (W == 4) {
         const float4 f = in ? __ldcs(reinterpret_cast<const float4*>(row + e0))
                             : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -170,7 +170,7 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k_rt, in
         int pos = incl - n;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-          if ((cmask >> i) & 1u) {
+          if (((cmask >> i) & 1u) && RF_IDX_OK(pos, 32)) {
             sm_val[warp][pos] = x[t][i];
             sm_idx[warp][pos] = expert(i);
             ++pos;
@@ -248,7 +248,7 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int k_rt, in
         if ((valid >> i) & 1u) l += __expf(x[t][i] - m);
       denom = gsum<G>(l, G);
     }
-    if (token < T && gl < k) {
+    if (token < T && gl < k && RF_IDX_OK((size_t)token * k + gl, (long long)T * k)) {
       idx_out[(size_t)token * k + gl] = myidx[t];
       w_out[(size_t)token * k + gl] = __fdividef(w, denom);
     }
@@ -276,7 +276,7 @@ __device__ __forceinline__ void load_token(const float* __restrict__ logits, int
 #pragma unroll
   for (int c = 0; c < NV / W; ++c) {
     const int e0 = c * G * W + gl * W;
-    const bool in = live && e0 < E;
+    const bool in = live && e0 < E && RF_SPAN_OK(e0, W, E) && RF_IDX_OK(token, T);
     if (W == 4) {
       const float4 f = in ? __ldcs(reinterpret_cast<const float4*>(row + e0))
                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -367,7 +367,7 @@ __device__ __forceinline__ void merge_select(const float (&x)[NV], int token, in
       for (int i = 0; i < NV; ++i) l += __expf(x[i] - m);
       denom = gsum<G>(l, G);
     }
-    if (token < T && gl < k) {
+    if (token < T && gl < k && RF_IDX_OK((size_t)token * k + gl, (long long)T * k)) {
       idx_out[(size_t)token * k + gl] = myidx;
       w_out[(size_t)token * k + gl] = __fdividef(w, denom);
     }
@@ -471,5 +471,7 @@ rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int reno
   }
   return launch_status();
 }
+
+RF_BOUNDS_WORD_OF_THIS_FILE
 
 }  // namespace rf

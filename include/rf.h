@@ -42,7 +42,9 @@ typedef enum {
   RF_ERR_UNSUPPORTED = 2,   /* a valid request outside the supported set      */
   RF_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned               */
   RF_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed    */
-  RF_ERR_TIMEOUT = 5        /* a bounded on-device wait gave up (see below)   */
+  RF_ERR_TIMEOUT = 5,       /* a bounded on-device wait gave up (see below)   */
+  RF_ERR_BOUNDS = 6         /* bounds-checked build only: an index was out of
+                               range and its access was skipped (see below)   */
 } rf_status;
 
 typedef enum { RF_F32 = 0, RF_BF16 = 1 } rf_dtype;
@@ -352,14 +354,35 @@ rf_status rf_rms_norm(const float* x, const float* gamma, int R, int n, float ep
 rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream);
 
 /*
- * rf_device_error -- status of the bounded on-device waits.  The
- * tensor-core kernels wait on shared-memory barriers with an iteration
- * limit; a wait that runs out records RF_ERR_TIMEOUT in a device word and
- * the kernel returns early instead of hanging.  This call synchronises
- * `stream`, reads that word into *status (RF_OK if no wait ran out), clears
- * it, and returns RF_OK, or RF_ERR_CUDA if the read failed.
+ * rf_device_error -- status of the on-device checks.  The tensor-core
+ * kernels wait on shared-memory barriers with an iteration limit; a wait
+ * that runs out records RF_ERR_TIMEOUT in a device word and the kernel
+ * returns early instead of hanging.  In the bounds-checked build (compiled
+ * with -DRF_CHECK_BOUNDS, see rf_bounds_checked) every kernel also checks
+ * each global-memory index against the extent of its buffer, derived from
+ * the call's sizes; an index out of range skips its load or store and
+ * records RF_ERR_BOUNDS.  This call synchronises `stream`, reads every such
+ * word into *status (RF_OK if nothing was recorded), clears them, and
+ * returns RF_OK, or RF_ERR_CUDA if the read failed.
  */
 rf_status rf_device_error(int* status, void* stream);
+
+/*
+ * rf_bounds_checked -- 1 if this library was built with -DRF_CHECK_BOUNDS
+ * (the debug variant whose kernels check every global index and report
+ * RF_ERR_BOUNDS through rf_device_error), else 0.
+ */
+int rf_bounds_checked(void);
+
+/*
+ * rf_selftest_bounds -- a self-test of the bounds checks.  A one-thread
+ * kernel presents one index equal to its buffer's extent (one past the end)
+ * to the same check every kernel uses; the check refuses it, so the guarded
+ * store, which would have gone to element 0 of an internal one-word buffer
+ * anyway, is skipped and RF_ERR_BOUNDS is recorded for rf_device_error.
+ * Errors: RF_ERR_UNSUPPORTED unless rf_bounds_checked() is 1.
+ */
+rf_status rf_selftest_bounds(void* stream);
 
 #ifdef __cplusplus
 }

@@ -38,3 +38,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _no_refused_index(request):
+    """Under the bounds-checked library (RF_LIBRARY names it), every GPU test
+    must also leave no refused index behind in rf_device_error."""
+    yield
+    if "gpu" not in request.keywords or not os.environ.get("RF_LIBRARY"):
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    import cascaded_reductions_gb300 as rf
+    if rf.rf_bounds_checked():
+        status = rf.rf_device_error()
+        assert status == rf.RF_OK, f"device status {status} after the test (6 = RF_ERR_BOUNDS)"

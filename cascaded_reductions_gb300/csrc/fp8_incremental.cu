@@ -19,11 +19,12 @@
 //   warp 0      TMA: bf16 X tiles (two 64-column boxes) and e4m3 Wq tiles
 //               (two 256-row boxes), 128-byte swizzle, 2-stage rings;
 //   warp 1      TMEM allocation and the MMAs (128x256x32, two per K-step);
-//   warps 2-9   two threads per row (one per 64-column half of the tile):
-//               partial abs-max, exchange with the other half (bounded
-//               mbarrier per row quarter), running scale, quantise into the
-//               swizzled A tile, rescale their half of the accumulator row
-//               when the scale grew, and finally the epilogue.
+//   warps 2-17  four threads per row (one per 32-column quarter of the
+//               tile; sixteen warps give the latency-bound conversion enough
+//               parallelism): partial abs-max, exchange with the other three
+//               (bounded mbarrier per row quarter), running scale, quantise
+//               into the swizzled A tile, rescale their quarter of the
+//               accumulator row when the scale grew, and finally the epilogue.
 // Every barrier wait is bounded (see tc_common.cuh).
 
 #include <cuda_bf16.h>
@@ -39,16 +40,18 @@ constexpr int STAGES = 2;
 constexpr int X_BYTES = BM * BK * 2;          // 32 KiB bf16 (two 16 KiB boxes)
 constexpr int W_BYTES = BN * BK;              // 64 KiB e4m3 (two 32 KiB boxes)
 constexpr int A_BYTES = BM * BK;              // 16 KiB e4m3
-constexpr int THREADS = 10 * 32;
+constexpr int PARTS = 4;                      // converter threads per row
+constexpr int CONV_WARPS = 4 * PARTS;
+constexpr int THREADS = (2 + CONV_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
 
 struct Shared {
   uint64_t x_full[STAGES], x_empty[STAGES];
   uint64_t w_full[STAGES], w_empty[STAGES];
   uint64_t a_full[STAGES], a_empty[STAGES];
-  uint64_t acc_done;
   uint64_t pair[4];
-  uint16_t pmax[2][2][BM];        // partial abs-max (a bf16 value), [step parity][half][row]
+  uint64_t pread[4];              // per row quarter: its PARTS warps have read pmax
+  uint16_t pmax[PARTS][BM];       // partial abs-max of the current tile (a bf16 value)
   uint32_t tmem_base;
   int abort;
 };
@@ -83,14 +86,16 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&sh->x_full[s], 1);
-      tc::mbar_init(&sh->x_empty[s], 8);
+      tc::mbar_init(&sh->x_empty[s], CONV_WARPS);
       tc::mbar_init(&sh->w_full[s], 1);
       tc::mbar_init(&sh->w_empty[s], 1);
-      tc::mbar_init(&sh->a_full[s], 8);
+      tc::mbar_init(&sh->a_full[s], CONV_WARPS);
       tc::mbar_init(&sh->a_empty[s], 1);
     }
-    tc::mbar_init(&sh->acc_done, 1);
-    for (int q = 0; q < 4; ++q) tc::mbar_init(&sh->pair[q], 2);
+    for (int q = 0; q < 4; ++q) {
+      tc::mbar_init(&sh->pair[q], PARTS);
+      tc::mbar_init(&sh->pread[q], PARTS);
+    }
     sh->abort = 0;
     tc::fence_barrier_init();
   }
@@ -143,12 +148,11 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
         }
         tc::mma_commit(&sh->a_empty[s]);
         tc::mma_commit(&sh->w_empty[s]);
-        tc::mma_commit(&sh->acc_done);
       }
     }
   } else {
     // ------------------------------------------------ quantise + rescale ----
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int quarter = warp & 3, part = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     float a = 0.f, s_cur = 0.f, rcp = 0.f;
@@ -160,33 +164,46 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
         ok = false;
         break;
       }
-      // this thread's 64 bf16 values of row r: box `half` of the X tile
-      uint4 xv[8];
-      const uint8_t* xb = sX + s * X_BYTES + half * (X_BYTES / 2);
+      // this thread's 32 bf16 values of row r: 16-byte chunks 4 (part % 2)
+      // to 4 (part % 2) + 3 of box part / 2 of the X tile
+      uint4 xv[4];
+      const uint8_t* xb = sX + s * X_BYTES + (part >> 1) * (X_BYTES / 2);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) xv[c] = *reinterpret_cast<const uint4*>(xb + sw128(r, c));
+      for (int c = 0; c < 4; ++c)
+        xv[c] = *reinterpret_cast<const uint4*>(xb + sw128(r, (part & 1) * 4 + c));
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->x_empty[s]);
-      // partial abs-max (packed bf16 pairs), then the other half's
-      uint32_t pk = 0u;
+      // partial abs-max (packed bf16 pairs, two chains), then the other parts'
+      uint32_t pk0 = 0u, pk1 = 0u;
       const uint32_t mask = 0x7FFF7FFFu;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk) : "r"(xv[c].x & mask));
-        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk) : "r"(xv[c].y & mask));
-        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk) : "r"(xv[c].z & mask));
-        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk) : "r"(xv[c].w & mask));
+      for (int c = 0; c < 4; ++c) {
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk0) : "r"(xv[c].x & mask));
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk1) : "r"(xv[c].y & mask));
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk0) : "r"(xv[c].z & mask));
+        asm("max.bf16x2 %0, %0, %1;" : "+r"(pk1) : "r"(xv[c].w & mask));
       }
-      const float pm = fmaxf(bf16_lo(pk), bf16_hi(pk));   // a bf16 value: exact in 16 bits
-      sh->pmax[t & 1][half][r] = (uint16_t)(__float_as_uint(pm) >> 16);
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(pk0) : "r"(pk1));
+      const float pm = fmaxf(bf16_lo(pk0), bf16_hi(pk0));  // a bf16 value: exact in 16 bits
+      // one pmax buffer: the other parts must have read the previous tile's
+      if (t > 0 && !tc::mbar_wait(&sh->pread[quarter], (uint32_t)(t - 1) & 1u, abort)) {
+        ok = false;
+        break;
+      }
+      sh->pmax[part][r] = (uint16_t)(__float_as_uint(pm) >> 16);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->pair[quarter]);
       if (!tc::mbar_wait(&sh->pair[quarter], (uint32_t)t & 1u, abort)) {
         ok = false;
         break;
       }
-      const float other = __uint_as_float((uint32_t)sh->pmax[t & 1][half ^ 1][r] << 16);
-      const float a_new = fmaxf(a, fmaxf(pm, other));
+      float tile_max = pm;
+#pragma unroll
+      for (int q = 0; q < PARTS; ++q)
+        tile_max = fmaxf(tile_max, __uint_as_float((uint32_t)sh->pmax[q][r] << 16));
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->pread[quarter]);
+      const float a_new = fmaxf(a, tile_max);
       // running scale; the accumulator is rescaled by s / s' when it grows
       float factor = 1.f;
       const bool grow = a > 0.f && a_new > a;
@@ -204,7 +221,7 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
       }
       uint8_t* ab = sA + s * A_BYTES;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         uint2 lo, hi;
         if (s_cur == 0.f) {
           lo = hi = make_uint2(0u, 0u);
@@ -215,20 +232,25 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
           lo = encode8_exact(xv[2 * j], s_cur);
           hi = encode8_exact(xv[2 * j + 1], s_cur);
         }
-        *reinterpret_cast<uint4*>(ab + sw128(r, 4 * half + j)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        *reinterpret_cast<uint4*>(ab + sw128(r, 2 * part + j)) = make_uint4(lo.x, lo.y, hi.x, hi.y);
       }
       // make the generic-proxy stores visible to the tensor core
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (t > 0) {
-        if (!tc::mbar_wait(&sh->acc_done, (uint32_t)(t - 1) & 1u, abort)) {
+      // a grown scale rescales the accumulator, which must then hold every
+      // earlier tile: wait for the MMAs of tile t-1 (the A stage they read is
+      // released when they finish).  Otherwise tile t is handed over at once
+      // and its MMAs queue behind those of tile t-1.
+      if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        const int sp = (t - 1) % STAGES;
+        if (!tc::mbar_wait(&sh->a_empty[sp], (uint32_t)((t - 1) / STAGES) & 1u, abort)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
+        {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t col = lane_base + (uint32_t)(half * 256 + c * 32);
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t col = lane_base + (uint32_t)(part * 128 + c * 32);
             uint32_t v[32];
             tc::tmem_ld_32x32b_x32(col, v);
             tc::tmem_ld_wait();
@@ -249,15 +271,17 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
       if (lane == 0) tc::mbar_arrive(&sh->a_full[s]);
     }
     // epilogue: Y = acc * s_final * sw
-    if (ok && tc::mbar_wait(&sh->acc_done, (uint32_t)(T - 1) & 1u, abort)) {
+    // every MMA has finished once the last tile's A stage is released
+    if (ok && tc::mbar_wait(&sh->a_empty[(T - 1) % STAGES], (uint32_t)((T - 1) / STAGES) & 1u,
+                            abort)) {
       tc::fence_after_sync();
       const int row = m0 + r;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(half * 256 + c * 32), v);
+        tc::tmem_ld_32x32b_x32(lane_base + (uint32_t)(part * 128 + c * 32), v);
         tc::tmem_ld_wait();
-        const int col0 = n0 + half * 256 + c * 32;
+        const int col0 = n0 + part * 128 + c * 32;
         if (!RF_SPAN_OK(col0, 32, N) || !RF_SPAN_OK((size_t)row * N + col0, 32, (long long)M * N))
           continue;                            // (checked build) sw and y spans
         uint32_t p[16];
@@ -274,7 +298,7 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
         for (int j = 0; j < 4; ++j)
           dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
       }
-      if (half == 0 && n0 == 0 && sx_out != nullptr && RF_IDX_OK(row, M)) sx_out[row] = s_cur;
+      if (part == 0 && n0 == 0 && sx_out != nullptr && RF_IDX_OK(row, M)) sx_out[row] = s_cur;
     }
   }
 

@@ -44,6 +44,7 @@ constexpr int PARTS = 4;                      // converter threads per row
 constexpr int CONV_WARPS = 4 * PARTS;
 constexpr int THREADS = (2 + CONV_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
+constexpr float kRcp448 = 1.0f / 448.0f;      // RN(1/448), folded by the compiler
 
 struct Shared {
   uint64_t x_full[STAGES], x_empty[STAGES];
@@ -208,10 +209,16 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
       float factor = 1.f;
       const bool grow = a > 0.f && a_new > a;
       if (a_new != a) {
-        const float s_new = __fdiv_rn(a_new, 448.f);
-        if (grow) factor = __fdiv_rn(s_cur, s_new);
-        s_cur = s_new;
+        // fp32(a' / 448) and fp32(s / s'), correctly rounded: the reciprocal
+        // and two residual corrections (see e4m3.cuh) where no residual can
+        // underflow, IEEE division otherwise
+        const float s_new =
+            a_new >= 0x1p-80f ? quotient(a_new, 448.f, kRcp448) : __fdiv_rn(a_new, 448.f);
         rcp = fast_scale(s_new) ? __frcp_rn(s_new) : 0.f;
+        if (grow)
+          factor = fast_scale(s_new) && s_cur >= s_new * 0x1p-64f ? quotient(s_cur, s_new, rcp)
+                                                                  : __fdiv_rn(s_cur, s_new);
+        s_cur = s_new;
         a = a_new;
       }
       // the A stage is free once the MMAs two tiles back have read it
@@ -247,24 +254,19 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
           break;
         }
         tc::fence_after_sync();
-        {
+        // this thread's 128 accumulator columns, 32 at a time (two loads in
+        // flight cost a register spill)
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t col = lane_base + (uint32_t)(part * 128 + c * 32);
-            uint32_t v[32];
-            tc::tmem_ld_32x32b_x32(col, v);
-            tc::tmem_ld_wait();
-            uint32_t w0[16], w1[16];
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t col = lane_base + (uint32_t)(part * 128 + c * 32);
+          uint32_t v[32];
+          tc::tmem_ld_32x32b_x32(col, v);
+          tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              w0[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
-              w1[i] = __float_as_uint(__uint_as_float(v[16 + i]) * factor);
-            }
-            tc::tmem_st_32x32b_x16(col, w0);
-            tc::tmem_st_32x32b_x16(col + 16u, w1);
-          }
-          tc::tmem_st_wait();
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
+          tc::tmem_st_32x32b_x32(col, v);
         }
+        tc::tmem_st_wait();
       }
       tc::fence_before_sync();
       __syncwarp();

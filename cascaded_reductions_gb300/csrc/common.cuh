@@ -81,15 +81,33 @@ struct Chunk<Bf16Tag> {
 // exp2(x - ref) is then 0 for x = -inf and the state stays the identity.
 __device__ __forceinline__ float ref_of(float m) { return m == -INFINITY ? 0.f : m; }
 
+// -------------------------------------------------------- status words ----
+// A translation unit that owns a device status word (the bounded-wait word of
+// the tensor-core files, the index-check word of the bounds-checked build)
+// registers a reader of it when the library loads; read_device_error calls
+// every registered reader, each of which reads and clears its word.
+using status_take_fn = rf_status (*)(int*);
+bool register_status_word(status_take_fn take);
+#define RF_STATUS_WORD_READER(fn, word)                                                     \
+  namespace {                                                                               \
+  rf_status fn(int* status) {                                                               \
+    int v = 0, zero = 0;                                                                    \
+    if (cudaMemcpyFromSymbol(&v, word, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;     \
+    if (cudaMemcpyToSymbol(word, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;    \
+    *status = v;                                                                            \
+    return RF_OK;                                                                           \
+  }                                                                                         \
+  const bool fn##_registered = register_status_word(&fn);                                   \
+  }
+
 // ------------------------------------------------------- bounds checks ----
 // Built with -DRF_CHECK_BOUNDS, every kernel checks each global load and
 // store against the extent of its buffer, computed in the kernel from the
 // call's size arguments (never from the pointer it is checking).  A refused
 // index skips its access (a load yields zeros) and records RF_ERR_BOUNDS in
-// this translation unit's device word; rf_device_error reads and clears the
-// words of every file through the functions registered with
-// register_bounds_word.  Without the flag RF_SPAN_OK is the constant true and
-// the checks compile to nothing.
+// this translation unit's device word, which the file registers with
+// RF_BOUNDS_WORD_OF_THIS_FILE.  Without the flag RF_SPAN_OK is the constant
+// true and the checks compile to nothing.
 #ifdef RF_CHECK_BOUNDS
 static __device__ int g_bounds_status;
 // elements [i, i + w) of a buffer of n elements
@@ -99,29 +117,12 @@ __device__ __forceinline__ bool span_ok(long long i, long long w, long long n) {
   return false;
 }
 #define RF_SPAN_OK(i, w, n) ::rf::span_ok((long long)(i), (long long)(w), (long long)(n))
-using bounds_take_fn = rf_status (*)(int*);
-bool register_bounds_word(bounds_take_fn take);
-#define RF_BOUNDS_WORD_OF_THIS_FILE                                                       \
-  namespace {                                                                             \
-  rf_status take_bounds_word(int* status) {                                               \
-    int v = 0, zero = 0;                                                                  \
-    if (cudaMemcpyFromSymbol(&v, g_bounds_status, sizeof(int)) != cudaSuccess)           \
-      return RF_ERR_CUDA;                                                                 \
-    if (cudaMemcpyToSymbol(g_bounds_status, &zero, sizeof(int)) != cudaSuccess)          \
-      return RF_ERR_CUDA;                                                                 \
-    *status = v;                                                                          \
-    return RF_OK;                                                                         \
-  }                                                                                       \
-  const bool g_bounds_word_registered = register_bounds_word(&take_bounds_word);          \
-  }
+#define RF_BOUNDS_WORD_OF_THIS_FILE RF_STATUS_WORD_READER(take_bounds_word, g_bounds_status)
 #else
 #define RF_SPAN_OK(i, w, n) true
 #define RF_BOUNDS_WORD_OF_THIS_FILE
 #endif
 #define RF_IDX_OK(i, n) RF_SPAN_OK(i, 1, n)
-// read-all-bounds-words half of rf_device_error (RF_OK with *status = 0 when
-// the build has no checks)
-rf_status take_bounds_words(int* status);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -174,18 +175,12 @@ rf_status launch_layer_norm(const float* x, const float* gamma, const float* bet
                             float eps, float* y, int level, float* work, cudaStream_t st);
 rf_status launch_fp8_incremental(const void* x, const uint8_t* wq, const float* sw, int M, int N,
                                  int K, void* y, float* sx_final, cudaStream_t st);
-rf_status fp8_incremental_take_status(int* status);
 rf_status launch_rms_norm(const float* x, const float* gamma, int R, int n, float eps, float* y,
                           int level, float* work, cudaStream_t st);
 rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, int S, float scale,
                             float* seg_m, float* seg_l, float* seg_acc, cudaStream_t st);
-rf_status mla_take_status(int* status);
 rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st);
-rf_status selftest_take_status(int* status);
 rf_status launch_selftest_bounds(cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);
-// read and clear the bounded-wait status word of each tensor-core kernel file
-rf_status gemm_take_status(int* status);
-rf_status prefill_take_status(int* status);
 
 }  // namespace rf

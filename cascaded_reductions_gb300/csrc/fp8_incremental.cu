@@ -330,13 +330,7 @@ rf_status launch_fp8_incremental(const void* x, const uint8_t* wq, const float* 
   return launch_status();
 }
 
-rf_status fp8_incremental_take_status(int* status) {
-  int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  *status = v;
-  return RF_OK;
-}
+RF_TIMEOUT_WORD_OF_THIS_FILE
 
 RF_BOUNDS_WORD_OF_THIS_FILE
 

@@ -266,13 +266,7 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
   return launch_status();
 }
 
-rf_status gemm_take_status(int* status) {
-  int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  *status = v;
-  return RF_OK;
-}
+RF_TIMEOUT_WORD_OF_THIS_FILE
 
 RF_BOUNDS_WORD_OF_THIS_FILE
 

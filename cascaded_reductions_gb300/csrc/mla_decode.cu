@@ -519,13 +519,7 @@ rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, i
   return launch_hg<16>(q, c, B, H, L, S, scale, seg_m, seg_l, seg_acc, st);
 }
 
-rf_status mla_take_status(int* status) {
-  int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  *status = v;
-  return RF_OK;
-}
+RF_TIMEOUT_WORD_OF_THIS_FILE
 
 RF_BOUNDS_WORD_OF_THIS_FILE
 

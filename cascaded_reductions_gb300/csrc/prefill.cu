@@ -451,13 +451,7 @@ rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int
   return launch_status();
 }
 
-rf_status prefill_take_status(int* status) {
-  int v = 0, zero = 0;
-  if (cudaMemcpyFromSymbol(&v, tc::g_timeout_status, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  if (cudaMemcpyToSymbol(tc::g_timeout_status, &zero, sizeof(int)) != cudaSuccess) return RF_ERR_CUDA;
-  *status = v;
-  return RF_OK;
-}
+RF_TIMEOUT_WORD_OF_THIS_FILE
 
 RF_BOUNDS_WORD_OF_THIS_FILE
 

@@ -12,8 +12,10 @@ namespace rf {
 namespace tc {
 
 // Each translation unit that includes this header gets its own status word;
-// a bounded wait that runs out stores RF_ERR_TIMEOUT into it.
+// a bounded wait that runs out stores RF_ERR_TIMEOUT into it, and the file
+// registers its reader with RF_TIMEOUT_WORD_OF_THIS_FILE.
 static __device__ int g_timeout_status;
+#define RF_TIMEOUT_WORD_OF_THIS_FILE RF_STATUS_WORD_READER(take_timeout_word, tc::g_timeout_status)
 
 // A wait gives up after this long (in %globaltimer nanoseconds).  Every
 // legitimate wait in these kernels lasts microseconds.

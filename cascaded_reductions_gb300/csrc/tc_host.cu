@@ -1,5 +1,5 @@
-// Host helpers of the tensor-core kernels: TMA descriptor encoding, SM count,
-// and the read-back of the bounded-wait status words.
+// Host helpers: TMA descriptor encoding and SM count for the tensor-core
+// kernels, and the registry and read-back of every device status word.
 #include <cudaTypedefs.h>
 
 #include <atomic>
@@ -45,48 +45,29 @@ int sm_count() {
 
 }  // namespace tc
 
-#ifdef RF_CHECK_BOUNDS
 namespace {
-// Filled during static initialisation of the library (one entry per kernel
-// file); zero-initialised storage, so registration order does not matter.
-constexpr int kMaxBoundsWords = 32;
-bounds_take_fn g_bounds_words[kMaxBoundsWords];
-std::atomic<int> g_n_bounds_words{0};
+// Filled during static initialisation of the library (one entry per status
+// word); zero-initialised storage, so registration order does not matter.
+constexpr int kMaxStatusWords = 32;
+status_take_fn g_status_words[kMaxStatusWords];
+std::atomic<int> g_n_status_words{0};
 }  // namespace
 
-bool register_bounds_word(bounds_take_fn take) {
-  const int i = g_n_bounds_words.fetch_add(1);
-  if (i < kMaxBoundsWords) g_bounds_words[i] = take;
-  return i < kMaxBoundsWords;
-}
-#endif
-
-rf_status take_bounds_words(int* status) {
-  *status = RF_OK;
-#ifdef RF_CHECK_BOUNDS
-  const int n = g_n_bounds_words.load() < kMaxBoundsWords ? g_n_bounds_words.load() : kMaxBoundsWords;
-  for (int i = 0; i < n; ++i) {
-    int w = RF_OK;
-    if (g_bounds_words[i](&w) != RF_OK) return RF_ERR_CUDA;
-    if (w != RF_OK && *status == RF_OK) *status = w;
-  }
-#endif
-  return RF_OK;
+bool register_status_word(status_take_fn take) {
+  const int i = g_n_status_words.fetch_add(1);
+  if (i < kMaxStatusWords) g_status_words[i] = take;
+  return i < kMaxStatusWords;
 }
 
 rf_status read_device_error(int* status, cudaStream_t st) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return RF_ERR_CUDA;
-  int st_words[6] = {0, 0, 0, 0, 0, 0};
-  if (gemm_take_status(&st_words[0]) != RF_OK || prefill_take_status(&st_words[1]) != RF_OK ||
-      fp8_incremental_take_status(&st_words[2]) != RF_OK || mla_take_status(&st_words[3]) != RF_OK ||
-      selftest_take_status(&st_words[4]) != RF_OK || take_bounds_words(&st_words[5]) != RF_OK)
-    return RF_ERR_CUDA;
   *status = RF_OK;
-  for (int w : st_words)
-    if (w != RF_OK) {
-      *status = w;
-      break;
-    }
+  const int n = g_n_status_words.load() < kMaxStatusWords ? g_n_status_words.load() : kMaxStatusWords;
+  for (int i = 0; i < n; ++i) {
+    int w = RF_OK;
+    if (g_status_words[i](&w) != RF_OK) return RF_ERR_CUDA;
+    if (w != RF_OK && *status == RF_OK) *status = w;      // every word is read and cleared
+  }
   return RF_OK;
 }
 

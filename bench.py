@@ -401,11 +401,16 @@ def path_single_row(torch, rf, peaks):
         rf.rf_attn_decode_split(q, K, V, S, scale, sm, sl, sa)
         rf.rf_state_merge(sm, sl, sa, out)
     ms = time_graph(torch, [call] * 50, 20)
+    counters = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fused = lambda: rf.rf_attn_decode_fused(q, K, V, S, scale, sm, sl, sa, counters, out)
+    ms_fused = time_graph(torch, [fused] * 50, 20)
     nbytes = 2 * cfg["L"] * cfg["D"] * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": "single-row decode fp32 q[64] K,V[4096,64], S=32 (latency bound; "
                         "graph of 50 back-to-back calls, inputs L2-resident)",
             "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+            "fused_us_per_call": round(ms_fused * 1e3, 2),
+            "fused_note": "rf_attn_decode_fused: the merge done by the row's last CTA, one launch",
             "roofline": roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", None)}
 
 
@@ -746,6 +751,23 @@ def run_rf(args):
 
     paths = {}
     if world == 1 and not args.decode_only:
+        # the same step as one launch: each row's last CTA merges its states
+        counters = torch.zeros(R, dtype=torch.int32, device="cuda")
+        fused = lambda: rf.rf_attn_decode_fused(q, K, V, S, scale, seg_m, seg_l, seg_acc, counters,
+                                                out, lse, stream)
+        for _ in range(3):
+            fused()
+        a, b = _events(torch, 2)
+        a.record(stream)
+        for _ in range(args.steps):
+            fused()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms_f = a.elapsed_time(b) / args.steps
+        paths["decode_fused_one_launch"] = {
+            "ms_per_step": round(ms_f, 4), "GB/s": round(job_gbs(kv_bytes, world, ms_f), 1),
+            "workload": "the headline step through rf_attn_decode_fused (split and merge in one "
+                        "launch, the merge done by each row's last CTA)"}
         paths["decode_incremental_vs_non_incremental"] = decode_ablation(torch, rf, peaks, q, K, V,
                                                                          scale)
         paths["decode_incremental_vs_non_incremental_short"] = decode_ablation_short(torch, rf, peaks)

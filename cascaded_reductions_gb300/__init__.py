@@ -55,6 +55,7 @@ _SIGNATURES = {
     "rf_mla_decode_split": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "rf_selftest_wait_timeout": (_I, [_P, _P]),
     "rf_rms_norm": (_I, [_P, _P, _I, _I, _F, _P, _I, _P, _P]),
+    "rf_attn_decode_fused": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _I, _P, _P]),
     "rf_bounds_checked": (_I, []),
     "rf_selftest_bounds": (_I, [_P]),
 }
@@ -135,6 +136,28 @@ def rf_attn_decode_split(q, k, v, S, scale, seg_m, seg_l, seg_acc, stream=None):
     _check(_lib.rf_attn_decode_split(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale),
                                      _dtype_code(k.dtype), _ptr(seg_m), _ptr(seg_l), _ptr(seg_acc),
                                      _stream(stream)), "rf_attn_decode_split")
+
+
+def rf_attn_decode_fused(q, k, v, S, scale, seg_m, seg_l, seg_acc, counters, out, lse=None,
+                         stream=None):
+    """Split-KV decode with the merge done by each row's last CTA, in one launch.
+    counters: int32 [R] CUDA tensor, zero before the first call (calls leave it zero)."""
+    R, L, D = k.shape
+    dt = _dtype_code(q.dtype)
+    _need(q, q.dtype, "q", (R, D))
+    _need(k, q.dtype, "k", (R, L, D))
+    _need(v, q.dtype, "v", (R, L, D))
+    _need(seg_m, torch.float32, "seg_m", (R, S))
+    _need(seg_l, torch.float32, "seg_l", (R, S))
+    _need(seg_acc, torch.float32, "seg_acc", (R, S, D))
+    _need(counters, torch.int32, "counters", (R,))
+    _need(out, out.dtype, "out", (R, D))
+    if lse is not None:
+        _need(lse, torch.float32, "lse", (R,))
+    _check(_lib.rf_attn_decode_fused(_ptr(q), _ptr(k), _ptr(v), R, L, D, S, float(scale), dt,
+                                     _ptr(seg_m), _ptr(seg_l), _ptr(seg_acc), _ptr(counters),
+                                     _ptr(out), _dtype_code(out.dtype), _ptr(lse), _stream(stream)),
+           "rf_attn_decode_fused")
 
 
 def rf_attn_decode_split_twopass(q, k, v, S, scale, seg_m, seg_l, seg_acc, stream=None):

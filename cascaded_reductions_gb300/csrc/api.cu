@@ -42,6 +42,24 @@ rf_status rf_attn_decode_split(const void* q, const void* k, const void* v, int 
                                  as_stream(stream));
 }
 
+rf_status rf_attn_decode_fused(const void* q, const void* k, const void* v, int R, int L, int D,
+                               int S, float scale, int dtype, float* seg_m, float* seg_l,
+                               float* seg_acc, int* counters, void* out, int out_dtype,
+                               float* lse, void* stream) {
+  if (!q || !k || !v || !seg_m || !seg_l || !seg_acc || !counters || !out)
+    return RF_ERR_INVALID_ARG;
+  if (R <= 0 || L <= 0 || D <= 0 || S < 1 || !isfinite(scale)) return RF_ERR_INVALID_ARG;
+  if (dtype != RF_F32 && dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (out_dtype != RF_F32 && out_dtype != RF_BF16) return RF_ERR_INVALID_ARG;
+  if (!((dtype == RF_F32 && D == 64) || (dtype == RF_BF16 && D == 128))) return RF_ERR_UNSUPPORTED;
+  if ((long long)R * S > 0x7fffffffLL) return RF_ERR_UNSUPPORTED;
+  if (!rf::aligned16(q) || !rf::aligned16(k) || !rf::aligned16(v) || !rf::aligned16(seg_acc) ||
+      !rf::aligned16(out) || !rf::aligned16(counters))
+    return RF_ERR_MISALIGNED;
+  return rf::launch_decode_fused(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                                 counters, out, out_dtype, lse, as_stream(stream));
+}
+
 rf_status rf_attn_decode_split_twopass(const void* q, const void* k, const void* v, int R, int L,
                                        int D, int S, float scale, int dtype, float* seg_m,
                                        float* seg_l, float* seg_acc, void* stream) {

@@ -152,6 +152,10 @@ inline rf_status launch_status() {
 rf_status launch_decode_split(const void* q, const void* k, const void* v, int R, int L, int D,
                               int S, float scale, int dtype, float* seg_m, float* seg_l,
                               float* seg_acc, cudaStream_t st);
+rf_status launch_decode_fused(const void* q, const void* k, const void* v, int R, int L, int D,
+                              int S, float scale, int dtype, float* seg_m, float* seg_l,
+                              float* seg_acc, int* counters, void* out, int out_dtype, float* lse,
+                              cudaStream_t st);
 rf_status launch_decode_twopass(const void* q, const void* k, const void* v, int R, int L, int D,
                                 int S, float scale, int dtype, float* seg_m, float* seg_l,
                                 float* seg_acc, cudaStream_t st);

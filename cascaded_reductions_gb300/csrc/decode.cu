@@ -27,17 +27,33 @@
 
 #include <math.h>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace rf {
 namespace {
 
-template <typename T, int WARPS, int U>
+// The fused form of the merge (FUSED): the CTA that finishes a row's last
+// segment merges that row's S states and writes out and lse.  Each CTA
+// publishes its state, fences, and counts itself in counters[row]; the CTA
+// that brings the count to S is the last, reads every state of the row
+// (written by the others before their own fence and count), merges them with
+// the same rescale as state_merge_kernel, and sets the counter back to 0 for
+// the next call.  No CTA waits for another.
+struct FusedMerge {
+  int* counters;       // [R], zero before the call, zero after it
+  void* out;           // [R, D], fp32 or bf16
+  float* lse;          // [R] or null
+  int out_bf16;
+};
+
+template <typename T, int WARPS, int U, bool FUSED>
 __global__ void __launch_bounds__(WARPS * 32)
 decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k,
                     const uint8_t* __restrict__ v, int L, int S, int seg_len, float scale_log2,
                     float* __restrict__ seg_m, float* __restrict__ seg_l,
-                    float* __restrict__ seg_acc) {
+                    float* __restrict__ seg_acc, FusedMerge fm) {
   constexpr int E = Chunk<T>::N;       // elements per 16-byte chunk
   constexpr int D = 16 * E;            // 16 chunks per 256-byte key row
   constexpr int ROW_BYTES = 256;
@@ -166,6 +182,43 @@ decode_split_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ k
       seg_l[state] = Lsum;
     }
   }
+  if constexpr (FUSED) {
+    // last arriver of the row merges: publish this segment, then count it
+    __shared__ int last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int seen = RF_IDX_OK(row, gridDim.x / S) ? atomicAdd(fm.counters + row, 1) : -1;
+      last = seen == S - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const size_t s0 = (size_t)row * S;
+    for (int d = threadIdx.x; d < D; d += WARPS * 32) {
+      // L2 reads (__ldcg): the states were written by other CTAs of this launch
+      float Mx = -INFINITY;
+      for (int s = 0; s < S; ++s) Mx = fmaxf(Mx, __ldcg(seg_m + s0 + s));
+      const float ref = Mx == -INFINITY ? 0.f : Mx;
+      float A = 0.f, Lsum = 0.f;
+      for (int s = 0; s < S; ++s) {
+        const float f = expf(__ldcg(seg_m + s0 + s) - ref);
+        Lsum = fmaf(f, __ldcg(seg_l + s0 + s), Lsum);
+        A = fmaf(f, __ldcg(seg_acc + (s0 + s) * D + d), A);
+      }
+      const float o = A / Lsum;
+      if (RF_IDX_OK((size_t)row * D + d, (long long)(gridDim.x / S) * D)) {
+        if (fm.out_bf16)
+          reinterpret_cast<__nv_bfloat16*>(fm.out)[(size_t)row * D + d] = __float2bfloat16_rn(o);
+        else
+          reinterpret_cast<float*>(fm.out)[(size_t)row * D + d] = o;
+      }
+      if (d == 0) {
+        if (fm.lse != nullptr) fm.lse[row] = Mx + logf(Lsum);
+        fm.counters[row] = 0;               // ready for the next call
+      }
+    }
+  }
 }
 
 // One warp per (row, 128-wide block of D) -- D/128 warps per row for D >= 128,
@@ -230,9 +283,10 @@ state_merge_kernel(const float* __restrict__ seg_m, const float* __restrict__ se
 
 }  // namespace
 
-rf_status launch_decode_split(const void* q, const void* k, const void* v, int R, int L, int D,
-                              int S, float scale, int dtype, float* seg_m, float* seg_l,
-                              float* seg_acc, cudaStream_t st) {
+template <bool FUSED>
+static rf_status launch_split_t(const void* q, const void* k, const void* v, int R, int L, int D, int S,
+                         float scale, int dtype, float* seg_m, float* seg_l, float* seg_acc,
+                         FusedMerge fm, cudaStream_t st) {
   const int seg_len = (L + S - 1) / S;
   const float sl2 = scale * kLog2e;
   const unsigned grid = (unsigned)R * (unsigned)S;
@@ -249,22 +303,37 @@ rf_status launch_decode_split(const void* q, const void* k, const void* v, int R
   const bool short_seg = seg_len <= 128 && grid >= 1024;   // many CTAs: occupancy decides
   if (dtype == RF_BF16 && D == 128) {
     if (short_seg)
-      decode_split_kernel<Bf16Tag, WARPS, 4><<<grid, WARPS * 32, 0, st>>>(
-          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+      decode_split_kernel<Bf16Tag, WARPS, 4, FUSED><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc, fm);
     else
-      decode_split_kernel<Bf16Tag, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(
-          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+      decode_split_kernel<Bf16Tag, WARPS, 8, FUSED><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc, fm);
   } else if (dtype == RF_F32 && D == 64) {
     if (short_seg)
-      decode_split_kernel<float, WARPS, 4><<<grid, WARPS * 32, 0, st>>>(
-          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+      decode_split_kernel<float, WARPS, 4, FUSED><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc, fm);
     else
-      decode_split_kernel<float, WARPS, 8><<<grid, WARPS * 32, 0, st>>>(
-          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc);
+      decode_split_kernel<float, WARPS, 8, FUSED><<<grid, WARPS * 32, 0, st>>>(
+          qb, kb, vb, L, S, seg_len, sl2, seg_m, seg_l, seg_acc, fm);
   } else {
     return RF_ERR_UNSUPPORTED;
   }
   return launch_status();
+}
+
+rf_status launch_decode_split(const void* q, const void* k, const void* v, int R, int L, int D,
+                              int S, float scale, int dtype, float* seg_m, float* seg_l,
+                              float* seg_acc, cudaStream_t st) {
+  return launch_split_t<false>(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                               FusedMerge{nullptr, nullptr, nullptr, 0}, st);
+}
+
+rf_status launch_decode_fused(const void* q, const void* k, const void* v, int R, int L, int D,
+                              int S, float scale, int dtype, float* seg_m, float* seg_l,
+                              float* seg_acc, int* counters, void* out, int out_dtype, float* lse,
+                              cudaStream_t st) {
+  return launch_split_t<true>(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                              FusedMerge{counters, out, lse, out_dtype == RF_BF16 ? 1 : 0}, st);
 }
 
 rf_status launch_state_merge(const float* seg_m, const float* seg_l, const float* seg_acc, int R,

@@ -221,6 +221,30 @@ rf_status rf_absmax_quant_fp8_gemm(const void* x, int M, int K,
                                    uint8_t* xq, float* sx, void* y, void* stream);
 
 /*
+ * rf_attn_decode_fused -- rf_attn_decode_split and rf_state_merge in one
+ * launch, for latency-bound calls (few rows, where the second launch costs
+ * as much as the work).  Every CTA writes its segment state as
+ * rf_attn_decode_split does, then counts itself in counters[row]; the CTA
+ * that completes a row's count merges that row's S states (the merge of
+ * rf_state_merge, transcript cue 21) into out and lse and sets the counter
+ * back to 0.  No CTA ever waits for another.
+ *   q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc
+ *            as rf_attn_decode_split (the states are written as there)
+ *   counters [R] int32, device memory: all 0 before the call; a call that
+ *            completes leaves them 0 again, so one zeroed buffer serves every
+ *            later call.  Calls that may overlap on the GPU need separate
+ *            counters and states.
+ *   out, out_dtype, lse  as rf_state_merge
+ * Errors: as rf_attn_decode_split, plus RF_ERR_INVALID_ARG for a null
+ * counters or out or a bad out_dtype, and RF_ERR_MISALIGNED unless out and
+ * counters are 16-byte aligned.
+ */
+rf_status rf_attn_decode_fused(const void* q, const void* k, const void* v, int R, int L, int D,
+                               int S, float scale, int dtype, float* seg_m, float* seg_l,
+                               float* seg_acc, int* counters, void* out, int out_dtype,
+                               float* lse, void* stream);
+
+/*
  * rf_attn_decode_noalloc -- rf_attn_decode_split followed by rf_state_merge
  * for callers that cannot allocate device memory: for example a plugin inside
  * a host engine that owns every device allocation, a latency-critical loop

@@ -58,6 +58,20 @@ NULL = P(0)
 F = ctypes.c_float
 
 
+def test_decode_fused_validation(lib):
+    f = lib.rf_attn_decode_fused
+    args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, o.get("R", 4), o.get("L", 100), o.get("D", 128),
+                        o.get("S", 4), F(o.get("scale", 0.1)), o.get("dtype", 1), FAKE, FAKE, FAKE,
+                        o.get("counters", FAKE), o.get("out", FAKE), o.get("out_dtype", 1), NULL, NULL]
+    assert f(*args(counters=NULL)) == 1
+    assert f(*args(out=NULL)) == 1
+    assert f(*args(out_dtype=5)) == 1
+    assert f(*args(S=0)) == 1
+    assert f(*args(D=64)) == 2            # bf16 with D=64 unsupported
+    assert f(*args(counters=ODD)) == 3
+    assert f(*args(out=ODD)) == 3
+
+
 def test_decode_split_validation(lib):
     f = lib.rf_attn_decode_split
     args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, o.get("R", 4), o.get("L", 100), o.get("D", 128),

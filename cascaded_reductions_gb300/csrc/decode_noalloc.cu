@@ -9,8 +9,10 @@
 // synchronisation is not acceptable, or a process whose device memory budget
 // was fixed at start-up.  This entry point keeps the segment states in a
 // fixed array that is part of the library image instead, so the call itself
-// allocates nothing: it only enqueues the same two kernels as the regular
-// path.
+// allocates nothing.  Up to kNoallocMaxRows rows it is one launch (the split
+// kernel with the merge done by each row's last CTA, counting in a second
+// fixed array of per-row counters that every completed call leaves at zero);
+// above that, the same two kernels as the regular path.
 //
 // Costs and rules of the shared array:
 //   * it is kRfNoallocScratchBytes (16 MiB) on every GPU that loads the
@@ -35,25 +37,34 @@ namespace rf {
 namespace {
 
 constexpr size_t kRfNoallocScratchBytes = 16u << 20;
+constexpr int kNoallocMaxRows = 65536;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kRfNoallocScratchBytes];
+// per-row counters of the one-launch merge: zero when the library loads, and
+// every completed call leaves them zero
+static __device__ __align__(256) int g_noalloc_counters[kNoallocMaxRows];
 
 std::mutex g_setup_mutex;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+int* g_counters_addr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (set-up on first use).
-rf_status scratch_address(void** out) {
+// Device addresses of the two arrays on the current device (set-up on first use).
+rf_status scratch_address(void** out, int** counters) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RF_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    void* c = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr ||
+        cudaGetSymbolAddress(&c, g_noalloc_counters) != cudaSuccess || c == nullptr)
       return RF_ERR_CUDA;
     g_scratch_addr[dev] = p;
+    g_counters_addr[dev] = static_cast<int*>(c);
   }
   *out = g_scratch_addr[dev];
+  *counters = g_counters_addr[dev];
   return RF_OK;
 }
 
@@ -78,12 +89,16 @@ extern "C" rf_status rf_attn_decode_noalloc(const void* q, const void* k, const 
   if (!rf::aligned16(q) || !rf::aligned16(k) || !rf::aligned16(v) || !rf::aligned16(out))
     return RF_ERR_MISALIGNED;
   void* base = nullptr;
-  rf_status s = rf::scratch_address(&base);
+  int* counters = nullptr;
+  rf_status s = rf::scratch_address(&base, &counters);
   if (s != RF_OK) return s;
   float* seg_m = static_cast<float*>(base);
   float* seg_l = seg_m + states;
   float* seg_acc = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + acc_off);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (R <= rf::kNoallocMaxRows)
+    return rf::launch_decode_fused(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                                   counters, out, out_dtype, lse, st);
   s = rf::launch_decode_split(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc, st);
   if (s != RF_OK) return s;
   return rf::launch_state_merge(seg_m, seg_l, seg_acc, R, S, D, out, out_dtype, lse, st);

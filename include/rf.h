@@ -256,7 +256,9 @@ rf_status rf_attn_decode_fused(const void* q, const void* k, const void* v, int 
  * out, out_dtype, lse as rf_state_merge.  The segment states live in a fixed
  * 16 MiB array inside the library (allocated once per GPU when the library
  * is loaded, kept until the process exits) instead of caller buffers, so the
- * call itself allocates nothing.
+ * call itself allocates nothing.  Up to 65536 rows the call is one launch,
+ * as rf_attn_decode_fused, with its per-row counters in a second fixed
+ * array; above that it launches the split and merge kernels.
  * - It needs 8*R*S bytes rounded up to 256, plus 4*R*S*D bytes, to fit in
  *   16 MiB; larger requests return RF_ERR_UNSUPPORTED with nothing launched.
  * - Every call on a GPU shares that array: calls that may overlap on the GPU

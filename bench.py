@@ -19,7 +19,10 @@ The same line carries:
                 workload, on the host's cores (one single-threaded worker per
                 core);
   clocks        nvidia-smi samples taken during the timed region;
-  paths         the other cascades (single-row fp32 decode, both routing
+  pages_claim   the speedup the pages claim for their own system, with the
+                hardware they name (context, not a target);
+  paths         the fused one-launch decode step on the same inputs, the
+                other cascades (single-row fp32 decode, both routing
                 shapes, quantisation, FP8 GEMM, causal prefill, MLA decode,
                 the single-row cascades at every fusion level, LayerNorm and
                 RMSNorm) and the incremental vs non-incremental decode
@@ -65,6 +68,17 @@ def measured_peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+# What the pages claim for their own system, as context beside the measured
+# numbers (not a target: the pages give speedups, no absolute throughput).
+PAGES_CLAIM = {
+    "speedup": "2x to 5x over state-of-the-art AI compilers (TVM, PyTorch Dynamo)",
+    "hardware": "NVIDIA A10 and H800",
+    "workloads": "multi-head attention, multi-latent attention, MoE routing, FP8 quantise + GEMM",
+    "source": "bookshelf explainer 'RedFuser: An Automatic Operator Fusion Framework for Cascaded "
+              "Reductions on AI Accelerators', section 'If you remember only three things', item 3",
+}
 
 
 def file_sha(path):
@@ -813,6 +827,7 @@ def run_rf(args):
             "gpu_launches": 2 * args.steps,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "pages_claim": PAGES_CLAIM,
             "paths": paths,
         }
         print(json.dumps(line), flush=True)

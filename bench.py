@@ -416,15 +416,24 @@ def path_single_row(torch, rf, peaks):
         rf.rf_state_merge(sm, sl, sa, out)
     ms = time_graph(torch, [call] * 50, 20)
     counters = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fused = lambda: rf.rf_attn_decode_fused(q, K, V, S, scale, sm, sl, sa, counters, out)
-    ms_fused = time_graph(torch, [fused] * 50, 20)
+    fused_sweep = {}
+    for Sf in (4, 8, 16, 32, 64):
+        smf = torch.empty(1, Sf, device="cuda")
+        slf = torch.empty(1, Sf, device="cuda")
+        saf = torch.empty(1, Sf, cfg["D"], device="cuda")
+        fused = lambda: rf.rf_attn_decode_fused(q, K, V, Sf, scale, smf, slf, saf, counters, out)
+        fused_sweep[f"S{Sf}"] = round(time_graph(torch, [fused] * 50, 20) * 1e3, 2)
+    best_fused = min(fused_sweep, key=fused_sweep.get)
+    ms_fused = fused_sweep[best_fused] * 1e-3
     nbytes = 2 * cfg["L"] * cfg["D"] * 4
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": "single-row decode fp32 q[64] K,V[4096,64], S=32 (latency bound; "
                         "graph of 50 back-to-back calls, inputs L2-resident)",
             "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
             "fused_us_per_call": round(ms_fused * 1e3, 2),
-            "fused_note": "rf_attn_decode_fused: the merge done by the row's last CTA, one launch",
+            "fused_note": f"rf_attn_decode_fused (the merge done by the row's last CTA, one "
+                          f"launch), best segment count {best_fused[1:]}",
+            "fused_us_by_segments": fused_sweep,
             "roofline": roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", None)}
 
 

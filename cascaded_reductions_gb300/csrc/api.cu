@@ -224,6 +224,10 @@ rf_status rf_incremental_quant_fp8_gemm(const void* x, int M, int K, const uint8
   if (M % 128 != 0 || N % 512 != 0 || K % 128 != 0) return RF_ERR_UNSUPPORTED;
   if (!rf::aligned16(x) || !rf::aligned16(wq) || !rf::aligned16(y) || !rf::aligned16(sw))
     return RF_ERR_MISALIGNED;
+  // clusters of 8 (or 4) CTAs share the quantisation where N allows it
+  const rf_status s =
+      rf::launch_fp8_incremental_cluster(x, wq, sw, M, N, K, y, sx_final, as_stream(stream));
+  if (s != RF_ERR_UNSUPPORTED) return s;
   return rf::launch_fp8_incremental(x, wq, sw, M, N, K, y, sx_final, as_stream(stream));
 }
 

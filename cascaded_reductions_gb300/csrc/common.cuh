@@ -179,6 +179,8 @@ rf_status launch_layer_norm(const float* x, const float* gamma, const float* bet
                             float eps, float* y, int level, float* work, cudaStream_t st);
 rf_status launch_fp8_incremental(const void* x, const uint8_t* wq, const float* sw, int M, int N,
                                  int K, void* y, float* sx_final, cudaStream_t st);
+rf_status launch_fp8_incremental_cluster(const void* x, const uint8_t* wq, const float* sw, int M,
+                                         int N, int K, void* y, float* sx_final, cudaStream_t st);
 rf_status launch_rms_norm(const float* x, const float* gamma, int R, int n, float eps, float* y,
                           int level, float* work, cudaStream_t st);
 rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, int S, float scale,

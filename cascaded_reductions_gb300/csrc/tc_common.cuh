@@ -234,6 +234,57 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// ------------------------------------------------------------- clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// every thread of every CTA of the cluster; orders shared-memory accesses
+// (local and remote) before it with those after it
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// the shared::cluster address of this CTA's shared-memory location
+// `smem_addr` as seen in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+
+// Bulk copy (async proxy) of `bytes` from this CTA's shared memory to another
+// CTA of the cluster: `dst` and `bar` are shared::cluster addresses (from
+// mapa) in that CTA; the copy completes as transaction bytes on `bar`.  Both
+// addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes,
+                                                  uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// generic-proxy writes to this CTA's shared memory before the fence are
+// ordered before later async-proxy accesses (tcgen05.mma operands, bulk copies)
+__device__ __forceinline__ void fence_proxy_async_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// mma_commit that arrives on the barrier at the same shared-memory offset in
+// every CTA of the cluster whose bit is set in `cta_mask`
+__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // ----------------------------------------------------------- descriptors ----
 // Shared-memory matrix descriptor for a tile stored in the 128-byte swizzle
 // layout (rows of 128 bytes, 8-row groups of 1024 bytes, 16-byte chunks

@@ -5,7 +5,10 @@ tolerance, the final per-row scales bit-exact.
 Cases: one K-tile; several tiles where the abs-max grows (outliers placed
 late, so the accumulator is rescaled); rows whose abs-max comes first (then
 the result equals the two-phase cascade's); zero rows and a zero prefix; and
-the full workload [4096 x 7168] x [4096 x 7168] on sampled rows."""
+the full workload [4096 x 7168] x [4096 x 7168] on sampled rows.  N = 512 and
+1024 run the one-CTA kernel; N = 2048 and 4096 run clusters of 4 and 8 CTAs
+that share the quantisation of each row band, so those shapes repeat the
+rescale and zero cases."""
 
 import numpy as np
 import pytest
@@ -47,24 +50,41 @@ def check(rf, x, wq, sw, what, rows=None):
     assert_close_bf16(gy, ry, what)
 
 
-@pytest.mark.parametrize("M,K,N", [(128, 128, 512), (256, 1024, 512), (128, 2048, 1024)])
+@pytest.mark.parametrize("M,K,N", [(128, 128, 512), (256, 1024, 512), (128, 2048, 1024),
+                                   (128, 128, 2048), (256, 896, 2048), (128, 128, 4096),
+                                   (256, 1280, 4096)])
 def test_shapes(rf, M, K, N):
     x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=M + K + N)
     check(rf, x, wq, sw, f"M={M} K={K} N={N}")
 
 
-def test_growing_abs_max_rescales(rf):
-    M, K, N = 128, 1024, 512
+@pytest.mark.parametrize("N", [512, 2048, 4096])
+def test_growing_abs_max_rescales(rf, N):
+    M, K = 128, 1024
     x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=21)
     xf = x.float()
     # the row maximum grows tile after tile: each later tile gets a larger outlier
     for t in range(K // 128):
         xf[:, t * 128 + 5] = 2.0 * (t + 1) * torch.sign(xf[:, t * 128 + 5] + 0.5)
-    check(rf, xf.to(torch.bfloat16), wq, sw, "growing")
+    check(rf, xf.to(torch.bfloat16), wq, sw, f"growing N={N}")
 
 
-def test_max_first_equals_two_phase(rf):
-    M, K, N = 128, 1024, 512
+@pytest.mark.parametrize("N", [2048, 4096])
+def test_growth_in_some_rows_only(rf, N):
+    # only a few rows grow, in different row bands and tiles: warps whose
+    # 32 rows did not grow leave their accumulator rows alone
+    M, K = 128, 1536
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=24)
+    xf = x.float()
+    for i, r in enumerate([3, 40, 77, 127]):
+        t = 2 + 3 * i
+        xf[r, t * 128 + 9] = 25.0 * (i + 1)
+    check(rf, xf.to(torch.bfloat16), wq, sw, f"some rows N={N}")
+
+
+@pytest.mark.parametrize("N", [512, 4096])
+def test_max_first_equals_two_phase(rf, N):
+    M, K = 128, 1024
     x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=22)
     xf = x.float()
     xf[:, 0] = 60.0
@@ -76,13 +96,14 @@ def test_max_first_equals_two_phase(rf):
     assert_close_bf16(gy, f64(y2), "vs two-phase")
 
 
-def test_zero_rows_and_zero_prefix(rf):
-    M, K, N = 128, 768, 512
+@pytest.mark.parametrize("N", [512, 4096])
+def test_zero_rows_and_zero_prefix(rf, N):
+    M, K = 128, 768
     x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=23)
     xf = x.float()
     xf[0] = 0.0
     xf[1, :300] = 0.0
-    check(rf, xf.to(torch.bfloat16), wq, sw, "zeros")
+    check(rf, xf.to(torch.bfloat16), wq, sw, f"zeros N={N}")
     gy, gs = run(rf, xf.to(torch.bfloat16), wq, sw)
     assert gs[0] == 0 and np.all(gy[0] == 0)
 

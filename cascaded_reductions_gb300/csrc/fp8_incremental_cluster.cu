@@ -27,10 +27,11 @@
 //   warp 1       TMEM allocation and the MMAs (128x256x32, one half of the
 //                accumulator at a time), committing A stages to every CTA of
 //                the cluster;
-//   warps 2-9    convert: 2C threads per owned row, running abs-max, encode
-//                into a 3-stage ring of A tiles; one of them loads the bf16 X
-//                bands (R rows, two 64-column boxes, 5- or 8-stage ring) and
-//                issues the copies to the cluster;
+//   warps 2-9    convert: 2C threads per owned row, each prefetching its own
+//                part of the bf16 X band with cp.async several tiles ahead
+//                (off the TMA unit, which the W tiles and the copies keep
+//                busy); running abs-max, encode into a 3-stage ring of A
+//                tiles; C - 1 lanes issue the copies to the cluster;
 //   warps 10-25  rescale each accumulator half when a row's scale grew (a
 //                warp whose 32 rows did not grow skips it), and the epilogue.
 // Every barrier wait is bounded (see tc_common.cuh).  The CTAs of a cluster
@@ -64,13 +65,12 @@ struct Cfg {
   static constexpr int R = BM / C;            // rows this CTA converts
   static constexpr int P = CONV_THREADS / R;  // converter threads per row (2C)
   static constexpr int E = BK / P;            // columns per converter thread (64 / C)
-  static constexpr int X_BYTES = R * BK * 2;  // one bf16 band: two boxes of R x 64
-  static constexpr int X_STAGES = C == 8 ? 8 : 5;  // deep: a band load takes ~2 us
+  static constexpr int X_BYTES = R * BK * 2;  // one bf16 band, each thread's part contiguous
+  static constexpr int X_STAGES = C == 8 ? 8 : 5;  // tiles of X in flight per thread
 };
 
 struct Shared {
   float2 fac[A_STAGES][BM];       // per A stage and row: {s / s' (1 if unchanged), s'}
-  uint64_t x_full[8];
   uint64_t w_full[W_STAGES], w_empty[W_STAGES];
   uint64_t a_full[A_STAGES];      // own band written + the other CTAs' bands copied in
   uint64_t a_empty[A_STAGES];     // one MMA commit from each CTA of the cluster
@@ -130,7 +130,7 @@ __device__ __forceinline__ void encode_row_part(const uint4 (&xv)[E / 8], float 
 
 template <int C>
 __global__ void __launch_bounds__(THREADS, 1)
-fp8_incremental_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
+fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
                                const __grid_constant__ CUtensorMap tmW,
                                const float* __restrict__ sw, __nv_bfloat16* __restrict__ y,
                                float* __restrict__ sx_out, int M, int N, int K) {
@@ -151,7 +151,6 @@ fp8_incremental_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
   const int band0 = (int)crank * G::R;          // first row this CTA converts
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < G::X_STAGES; ++s) tc::mbar_init(&sh->x_full[s], 1);
     for (int s = 0; s < A_STAGES; ++s) {
       tc::mbar_init(&sh->a_full[s], 1);
       tc::mbar_init(&sh->a_empty[s], C);
@@ -226,30 +225,36 @@ fp8_incremental_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
     const int col = j * G::E;                    // first column of the part
     const int row = band0 + br;                  // row of the 128-row block
     constexpr uint32_t BAND_BYTES = G::R * BK, FAC_BYTES = G::R * sizeof(float2);
+    // this thread's E values of tile t: 16-byte chunk u at u * CONV_THREADS * 16
+    // + ct * 16 of the stage (each LDS.128 of the warp reads 512 contiguous bytes)
+    const __nv_bfloat16* xrow = x + (size_t)(m0 + row) * K + col;
     auto load_x = [&](int t) {
-      const int s = t % G::X_STAGES;
-      tc::mbar_arrive_expect_tx(&sh->x_full[s], G::X_BYTES);
-      tc::tma_load_2d(sX + s * G::X_BYTES, &tmX, &sh->x_full[s], t * BK, m0 + band0);
-      tc::tma_load_2d(sX + s * G::X_BYTES + G::X_BYTES / 2, &tmX, &sh->x_full[s], t * BK + 64,
-                      m0 + band0);
+      if (t < T) {
+        uint8_t* dst = sX + (t % G::X_STAGES) * G::X_BYTES + ct * 16;
+#pragma unroll
+        for (int u = 0; u < G::E / 8; ++u)
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                           tc::smem_u32(dst + u * CONV_THREADS * 16)),
+                       "l"(xrow + (size_t)t * BK + u * 8)
+                       : "memory");
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");   // (empty past the end)
     };
-    if (ct == 0) {
-      tc::prefetch_tmap(&tmX);
-      for (int t = 0; t < T && t < G::X_STAGES; ++t) load_x(t);
-    }
+    for (int t = 0; t < G::X_STAGES; ++t) load_x(t);
     float a = 0.f, s_cur = 0.f, rcp = 0.f;
     bool ok = T > 0;
     for (int t = 0; t < T && ok; ++t) {
       const int s = t % A_STAGES;
       const uint32_t ph = (uint32_t)(t / A_STAGES) & 1u;
-      const int xs = t % G::X_STAGES;
-      bool good = warp_wait(&sh->x_full[xs], (uint32_t)(t / G::X_STAGES) & 1u, abort);
-      if (good) {
+      // this thread's copies of tile t are the oldest of X_STAGES groups
+      asm volatile("cp.async.wait_group %0;" ::"n"(G::X_STAGES - 1) : "memory");
+      bool good = true;
+      {
         uint4 xv[G::E / 8];
-        const uint8_t* xb = sX + xs * G::X_BYTES + (col / 64) * (G::X_BYTES / 2);
+        const uint8_t* xb = sX + (t % G::X_STAGES) * G::X_BYTES + ct * 16;
 #pragma unroll
         for (int u = 0; u < G::E / 8; ++u)
-          xv[u] = *reinterpret_cast<const uint4*>(xb + sw128(br, (col % 64) / 8 + u));
+          xv[u] = *reinterpret_cast<const uint4*>(xb + u * CONV_THREADS * 16);
         // abs-max of the part (packed bf16 pairs), then over the row's P threads
         uint32_t pk = 0u;
         const uint32_t mask = 0x7FFF7FFFu;
@@ -280,6 +285,8 @@ fp8_incremental_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
         }
         uint2 codes[G::E / 8];
         encode_row_part<G::E>(xv, s_cur, rcp, codes);
+        // the values read from X stage t % X_STAGES are consumed: refill it
+        load_x(t + G::X_STAGES);
         // A stage s is free once every CTA's MMAs of tile t - A_STAGES have read it
         good = warp_wait(&sh->a_empty[s], ph ^ 1u, abort);
         if (good) {
@@ -298,27 +305,23 @@ fp8_incremental_cluster_kernel(const __grid_constant__ CUtensorMap tmX,
       // the band is read by this CTA's tensor core and by the bulk copies
       tc::fence_proxy_async_cta();
       ok = converters_sync_and(good);
-      if (ok && ct == 0) {
-        // the band and its factors to every other CTA of the cluster, then
-        // this CTA's own arrival, expecting the other CTAs' bands
-        const uint8_t* band = sA + s * A_BYTES + band0 * BK;
-        const float2* fband = &sh->fac[s][band0];
-        const uint32_t band_off = (uint32_t)(band - smem);
-        const uint32_t fac_off = (uint32_t)(reinterpret_cast<const uint8_t*>(fband) - smem);
-        const uint32_t bar = tc::smem_u32(&sh->a_full[s]);
-        const uint32_t base = tc::smem_u32(smem);
-#pragma unroll 1
-        for (uint32_t p = 1; p < (uint32_t)C; ++p) {
-          const uint32_t peer = (crank + p) % (uint32_t)C;
-          const uint32_t peer_bar = tc::mapa(bar, peer);
-          tc::bulk_copy_to_peer(tc::mapa(base + band_off, peer), band, BAND_BYTES, peer_bar);
-          tc::bulk_copy_to_peer(tc::mapa(base + fac_off, peer), fband, FAC_BYTES, peer_bar);
+      if (ok && ct < C) {
+        if (ct == 0) {
+          // this CTA's own arrival, expecting the other CTAs' bands
+          tc::mbar_arrive_expect_tx(&sh->a_full[s],
+                                    (uint32_t)(C - 1) * (BAND_BYTES + FAC_BYTES));
+        } else {
+          // lane ct sends the band and its factors to CTA crank + ct (mod C)
+          const uint8_t* band = sA + s * A_BYTES + band0 * BK;
+          const float2* fband = &sh->fac[s][band0];
+          const uint32_t peer = (crank + (uint32_t)ct) % (uint32_t)C;
+          const uint32_t peer_bar = tc::mapa(tc::smem_u32(&sh->a_full[s]), peer);
+          tc::bulk_copy_to_peer(tc::mapa(tc::smem_u32(band), peer), band, BAND_BYTES, peer_bar);
+          tc::bulk_copy_to_peer(tc::mapa(tc::smem_u32(fband), peer), fband, FAC_BYTES, peer_bar);
         }
-        tc::mbar_arrive_expect_tx(&sh->a_full[s], (uint32_t)(C - 1) * (BAND_BYTES + FAC_BYTES));
-        // every converter has read X stage xs: load tile t + X_STAGES into it
-        if (t + G::X_STAGES < T) load_x(t + G::X_STAGES);
       }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");   // no copy outlives the loop
     // the last A_STAGES tiles' MMA commits of every CTA target this CTA's
     // a_empty barriers: let them land before the cluster barrier
     if (ok && ct == 0) {
@@ -428,45 +431,43 @@ cudaLaunchConfig_t cluster_config(cudaLaunchAttribute* attr, unsigned grid, cuda
   return cfg;
 }
 
-// Whether clusters of C of these CTAs can be resident on the current device
-// (queried once per device); also sets the kernel's shared-memory attribute.
+// How many clusters of C of these CTAs can be resident at once on the current
+// device (0: none), queried once per device (up to 64); also sets the
+// kernel's shared-memory attribute.
 template <int C>
-bool cluster_fits() {
-  static std::atomic<uint64_t> attr_done{0}, known{0}, fits{0};
+int resident_clusters() {
+  static std::atomic<int> count[64];
+  static std::atomic<uint64_t> attr_done{0}, known{0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return false;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const uint64_t bit = 1ull << dev;
-  if (known.load(std::memory_order_acquire) & bit)
-    return (fits.load(std::memory_order_acquire) & bit) != 0;
-  if (smem_attr(fp8_incremental_cluster_kernel<C>, smem_bytes<C>(), attr_done) != RF_OK) {
-    cudaGetLastError();
-    return false;
-  }
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = cluster_config<C>(attr, (unsigned)C, 0);
+  if (known.load(std::memory_order_acquire) & bit) return count[dev].load();
   int n = 0;
-  const bool ok = cudaOccupancyMaxActiveClusters(&n, fp8_incremental_cluster_kernel<C>, &cfg) ==
-                      cudaSuccess &&
-                  n > 0;
-  if (!ok) cudaGetLastError();
-  if (ok) fits.fetch_or(bit, std::memory_order_release);
+  if (smem_attr(fp8_incremental_cluster_kernel<C>, smem_bytes<C>(), attr_done) == RF_OK) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = cluster_config<C>(attr, (unsigned)C, 0);
+    if (cudaOccupancyMaxActiveClusters(&n, fp8_incremental_cluster_kernel<C>, &cfg) !=
+        cudaSuccess)
+      n = 0;
+  }
+  cudaGetLastError();
+  count[dev].store(n);
   known.fetch_or(bit, std::memory_order_release);
-  return ok;
+  return n;
 }
 
 template <int C>
 rf_status launch_c(const void* x, const uint8_t* wq, const float* sw, int M, int N, int K,
                    void* y, float* sx_final, cudaStream_t st) {
-  CUtensorMap tx, tw;
-  if (!tc::make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, (uint64_t)K, (uint64_t)M,
-                        (uint64_t)K * 2, 64, Cfg<C>::R, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
+  CUtensorMap tw;
+  if (!tc::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K, BK, 256, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
   const unsigned grid = (unsigned)(M / BM) * (unsigned)(N / BN);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config<C>(attr, grid, st);
-  if (cudaLaunchKernelEx(&cfg, fp8_incremental_cluster_kernel<C>, tx, tw, sw,
+  if (cudaLaunchKernelEx(&cfg, fp8_incremental_cluster_kernel<C>,
+                         static_cast<const __nv_bfloat16*>(x), tw, sw,
                          static_cast<__nv_bfloat16*>(y), sx_final, M, N, K) != cudaSuccess) {
     cudaGetLastError();
     return RF_ERR_CUDA;
@@ -476,17 +477,24 @@ rf_status launch_c(const void* x, const uint8_t* wq, const float* sw, int M, int
 
 }  // namespace
 
-// Launches the cluster kernel when N / 512 is a multiple of 8 (or 4) and such
+// Launches the cluster kernel when N / 512 is a multiple of 4 and such
 // clusters fit on the device; returns RF_ERR_UNSUPPORTED otherwise, leaving
-// the shape to the one-CTA kernel.
+// the shape to the one-CTA kernel.  Of the cluster sizes that divide N / 512,
+// the one whose grid runs in fewer waves of resident CTAs is taken (fewer 8-CTA
+// clusters than 4-CTA ones fit on the GPU's processing clusters); on a tie,
+// 8, which converts fewer rows per CTA.
 rf_status launch_fp8_incremental_cluster(const void* x, const uint8_t* wq, const float* sw, int M,
                                          int N, int K, void* y, float* sx_final,
                                          cudaStream_t st) {
+  const long long grid = (long long)(M / BM) * (N / BN);
   const int nblocks = N / BN;
-  if (nblocks % 8 == 0 && cluster_fits<8>())
-    return launch_c<8>(x, wq, sw, M, N, K, y, sx_final, st);
-  if (nblocks % 4 == 0 && cluster_fits<4>())
-    return launch_c<4>(x, wq, sw, M, N, K, y, sx_final, st);
+  auto waves = [&](int c, int clusters) {
+    return clusters > 0 ? (grid + (long long)c * clusters - 1) / ((long long)c * clusters) : -1;
+  };
+  const long long w8 = nblocks % 8 == 0 ? waves(8, resident_clusters<8>()) : -1;
+  const long long w4 = nblocks % 4 == 0 ? waves(4, resident_clusters<4>()) : -1;
+  if (w8 > 0 && (w4 <= 0 || w8 <= w4)) return launch_c<8>(x, wq, sw, M, N, K, y, sx_final, st);
+  if (w4 > 0) return launch_c<4>(x, wq, sw, M, N, K, y, sx_final, st);
   return RF_ERR_UNSUPPORTED;
 }
 

@@ -6,9 +6,10 @@ Cases: one K-tile; several tiles where the abs-max grows (outliers placed
 late, so the accumulator is rescaled); rows whose abs-max comes first (then
 the result equals the two-phase cascade's); zero rows and a zero prefix; and
 the full workload [4096 x 7168] x [4096 x 7168] on sampled rows.  N = 512 and
-1024 run the one-CTA kernel; N = 2048 and 4096 run clusters of 4 and 8 CTAs
-that share the quantisation of each row band, so those shapes repeat the
-rescale and zero cases."""
+1024 run the one-CTA kernel; N = 2048 runs clusters of 4 CTAs and N = 4096
+with few rows clusters of 8 (the full workload takes clusters of 4, which
+need fewer waves), each CTA quantising one row band for the cluster, so
+those shapes repeat the rescale and zero cases."""
 
 import numpy as np
 import pytest

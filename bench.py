@@ -509,13 +509,19 @@ def path_gemm(torch, rf, peaks):
     nrm = exact.norm().item()
     err_two = (y[rows].double() - exact).norm().item() / nrm
     err_inc = (y_inc[rows].double() - exact).norm().item() / nrm
+    tf_inc = 2.0 * M * N * K / (ms_inc * 1e-3) / 1e12
     incremental = {"us_per_call": round(ms_inc * 1e3, 2),
+                   "TFLOP/s": round(tf_inc, 1),
                    "us_two_phase_quant_plus_gemm": round(ms_both * 1e3, 2),
                    "rel_error_vs_exact_product": round(err_inc, 6),
                    "rel_error_two_phase": round(err_two, 6),
+                   "roofline": roofline("tensor", tf_inc, fp8_peak, "TFLOP/s",
+                                        ncu_traffic("fp8_incremental_cluster")),
                    "workload": f"one kernel: bf16 X [{M} x {K}] read in 128-column tiles, running "
                                f"abs-max, e4m3 tiles in shared memory, accumulator rescaled when the "
-                               f"scale grows; error = Frobenius norm over 64 rows"}
+                               f"scale grows; clusters of CTAs that share a 128-row block quantise "
+                               f"one row band each and copy the codes to the others; "
+                               f"error = Frobenius norm over 64 rows"}
     return {"incremental_quant_gemm": incremental,
             "workload": f"FP8 GEMM Y[{M} x {N}] = Xq[{M} x {K}] Wq^T, e4m3, fp32 accumulate, bf16 out",
             "value": round(tf, 1), "unit": "TFLOP/s", "us_per_call": round(ms * 1e3, 2),

@@ -15,10 +15,11 @@
 // A cluster of C CTAs (C = 8 or 4) covers C consecutive 512-column blocks of
 // one 128-row block of Y.  CTA c of the cluster owns rows [c R, c R + R),
 // R = 128 / C: it alone reads those rows of X, keeps their running abs-max,
-// encodes them into its own A tile, and bulk-copies that band of codes and
-// the band's per-row factors s / s' into the A tile of every other CTA of the
-// cluster (distributed shared memory); the copies complete on the receiving
-// CTA's A barrier.  Each CTA thus quantises 1/C of the tile instead of all.
+// encodes them into its own A tile, and stores the codes and the rows'
+// factors s / s' into the A tile of every other CTA of the cluster too
+// (st.async into distributed shared memory, completing as transaction bytes
+// on the receiving CTA's A barrier).  Each CTA thus quantises 1/C of the
+// tile instead of all of it.
 //
 // One CTA per 128 x 512 block of Y; 512 TMEM columns hold the accumulator as
 // two halves of 256 columns, so that one half is rescaled while the tensor
@@ -29,9 +30,10 @@
 //                the cluster;
 //   warps 2-9    convert: 2C threads per owned row, each prefetching its own
 //                part of the bf16 X band with cp.async several tiles ahead
-//                (off the TMA unit, which the W tiles and the copies keep
-//                busy); running abs-max, encode into a 3-stage ring of A
-//                tiles; C - 1 lanes issue the copies to the cluster;
+//                (off the TMA unit, which the W tiles keep busy); running
+//                abs-max, encode into a 4-stage ring of A tiles, every
+//                thread storing its codes into all C of them; each warp
+//                runs on without waiting for the others;
 //   warps 10-25  rescale each accumulator half when a row's scale grew (a
 //                warp whose 32 rows did not grow skips it), and the epilogue.
 // Every barrier wait is bounded (see tc_common.cuh).  The CTAs of a cluster
@@ -49,13 +51,14 @@ namespace rf {
 namespace {
 
 constexpr int BM = 128, BN = 512, BK = 128;
-constexpr int A_STAGES = 3, W_STAGES = 4;
+constexpr int A_STAGES = 4, W_STAGES = 4;
 constexpr int W_BYTES = 256 * BK;             // one 256-row half of the Wq tile, e4m3
 constexpr int A_BYTES = BM * BK;              // 16 KiB e4m3
+constexpr int FIRST_CONV_WARP = 2;
 constexpr int CONV_WARPS = 8, RESC_WARPS = 16;
 constexpr int CONV_THREADS = CONV_WARPS * 32;
-constexpr int FIRST_RESC_WARP = 2 + CONV_WARPS;
-constexpr int THREADS = (2 + CONV_WARPS + RESC_WARPS) * 32;
+constexpr int FIRST_RESC_WARP = FIRST_CONV_WARP + CONV_WARPS;
+constexpr int THREADS = (FIRST_RESC_WARP + RESC_WARPS) * 32;
 constexpr int TMEM_COLS = 512;
 constexpr float kRcp448 = 1.0f / 448.0f;      // RN(1/448), folded by the compiler
 
@@ -66,13 +69,13 @@ struct Cfg {
   static constexpr int P = CONV_THREADS / R;  // converter threads per row (2C)
   static constexpr int E = BK / P;            // columns per converter thread (64 / C)
   static constexpr int X_BYTES = R * BK * 2;  // one bf16 band, each thread's part contiguous
-  static constexpr int X_STAGES = C == 8 ? 8 : 5;  // tiles of X in flight per thread
+  static constexpr int X_STAGES = C == 8 ? 4 : 3;  // tiles of X in flight per thread
 };
 
 struct Shared {
   float2 fac[A_STAGES][BM];       // per A stage and row: {s / s' (1 if unchanged), s'}
   uint64_t w_full[W_STAGES], w_empty[W_STAGES];
-  uint64_t a_full[A_STAGES];      // own band written + the other CTAs' bands copied in
+  uint64_t a_full[A_STAGES];      // own band written + the other CTAs' bands stored in
   uint64_t a_empty[A_STAGES];     // one MMA commit from each CTA of the cluster
   uint64_t mma_done[2];           // per accumulator half
   uint64_t resc_done[2];          // per accumulator half: the rescale warps
@@ -91,21 +94,6 @@ static_assert(smem_bytes<4>() <= 232448 && smem_bytes<8>() <= 232448,
 // byte offset of 16-byte chunk `c` of row `r` in a 128-byte-swizzled tile
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
-// barrier of the converter warps that also ANDs `v` over them, so that every
-// converter leaves the tile loop at the same tile (none is left waiting here)
-__device__ __forceinline__ bool converters_sync_and(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "n"(CONV_THREADS)
-      : "memory");
-  return r != 0;
 }
 
 // a bounded wait whose outcome is the same for every lane of the warp
@@ -152,7 +140,7 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < A_STAGES; ++s) {
-      tc::mbar_init(&sh->a_full[s], 1);
+      tc::mbar_init(&sh->a_full[s], CONV_WARPS);
       tc::mbar_init(&sh->a_empty[s], C);
     }
     for (int q = 0; q < W_STAGES; ++q) {
@@ -195,6 +183,8 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
         const int s = t % A_STAGES;
         const uint32_t ph = (uint32_t)(t / A_STAGES) & 1u;
         if (!(ok = tc::mbar_wait(&sh->a_full[s], ph, abort))) break;
+        // the other CTAs' codes were stored into this stage by st.async
+        tc::fence_proxy_async_cta();
         const uint32_t a_addr = tc::smem_u32(sA + s * A_BYTES);
         for (int h = 0; h < 2; ++h) {
           const int i = 2 * t + h, q = i % W_STAGES;
@@ -219,15 +209,21 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
     }
   } else if (warp < FIRST_RESC_WARP) {
     // -------------------------------------------------------- convert ----
-    const int ct = threadIdx.x - 64;             // 0 .. CONV_THREADS-1
+    const int ct = threadIdx.x - FIRST_CONV_WARP * 32;   // 0 .. CONV_THREADS-1
     const int br = ct / G::P;                    // row of this CTA's band
     const int j = ct % G::P;                     // part of the row
     const int col = j * G::E;                    // first column of the part
     const int row = band0 + br;                  // row of the 128-row block
-    constexpr uint32_t BAND_BYTES = G::R * BK, FAC_BYTES = G::R * sizeof(float2);
     // this thread's E values of tile t: 16-byte chunk u at u * CONV_THREADS * 16
     // + ct * 16 of the stage (each LDS.128 of the warp reads 512 contiguous bytes)
     const __nv_bfloat16* xrow = x + (size_t)(m0 + row) * K + col;
+    constexpr uint32_t BAND_BYTES = G::R * BK, FAC_BYTES = G::R * sizeof(float2);
+    // shared::cluster address of this shared memory in the other CTAs, for
+    // p = 1 .. C-1 (CTA crank + p mod C)
+    const uint32_t base = tc::smem_u32(smem);
+    uint32_t peer[C];
+#pragma unroll
+    for (int p = 1; p < C; ++p) peer[p] = tc::mapa(base, (crank + (uint32_t)p) % (uint32_t)C);
     auto load_x = [&](int t) {
       if (t < T) {
         uint8_t* dst = sX + (t % G::X_STAGES) * G::X_BYTES + ct * 16;
@@ -300,25 +296,36 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
                   make_uint4(codes[2 * u].x, codes[2 * u].y, codes[2 * u + 1].x, codes[2 * u + 1].y);
           }
           if (j == 0) sh->fac[s][row] = make_float2(factor, s_cur);
+          // the same codes and factors into the other CTAs' stage s
+          const uint32_t code_off = tc::smem_u32(ab + sw128(row, col / 16) + col % 16) - base;
+          const uint32_t fac_off = tc::smem_u32(&sh->fac[s][row]) - base;
+          const uint32_t bar_off = tc::smem_u32(&sh->a_full[s]) - base;
+#pragma unroll
+          for (int p = 1; p < C; ++p) {
+            if constexpr (G::E == 8)
+              tc::st_async_v2(peer[p] + code_off, codes[0].x, codes[0].y, peer[p] + bar_off);
+            else
+              tc::st_async_v4(peer[p] + code_off,
+                              make_uint4(codes[0].x, codes[0].y, codes[1].x, codes[1].y),
+                              peer[p] + bar_off);
+            if (j == 0)
+              tc::st_async_v2(peer[p] + fac_off, __float_as_uint(factor), __float_as_uint(s_cur),
+                              peer[p] + bar_off);
+          }
         }
       }
-      // the band is read by this CTA's tensor core and by the bulk copies
+      // this CTA's tensor core reads the band through the async proxy
       tc::fence_proxy_async_cta();
-      ok = converters_sync_and(good);
-      if (ok && ct < C) {
-        if (ct == 0) {
-          // this CTA's own arrival, expecting the other CTAs' bands
+      __syncwarp();
+      if (!(ok = good)) break;
+      // one arrival per converter warp; the first also expects the other
+      // CTAs' bands
+      if (lane == 0) {
+        if (warp == FIRST_CONV_WARP)
           tc::mbar_arrive_expect_tx(&sh->a_full[s],
                                     (uint32_t)(C - 1) * (BAND_BYTES + FAC_BYTES));
-        } else {
-          // lane ct sends the band and its factors to CTA crank + ct (mod C)
-          const uint8_t* band = sA + s * A_BYTES + band0 * BK;
-          const float2* fband = &sh->fac[s][band0];
-          const uint32_t peer = (crank + (uint32_t)ct) % (uint32_t)C;
-          const uint32_t peer_bar = tc::mapa(tc::smem_u32(&sh->a_full[s]), peer);
-          tc::bulk_copy_to_peer(tc::mapa(tc::smem_u32(band), peer), band, BAND_BYTES, peer_bar);
-          tc::bulk_copy_to_peer(tc::mapa(tc::smem_u32(fband), peer), fband, FAC_BYTES, peer_bar);
-        }
+        else
+          tc::mbar_arrive(&sh->a_full[s]);
       }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");   // no copy outlives the loop

@@ -269,6 +269,23 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
       : "memory");
 }
 
+// Asynchronous store of 8 or 16 bytes into another CTA of the cluster (`dst`
+// and `bar` shared::cluster addresses from mapa, `dst` aligned to the size),
+// completing as transaction bytes on that CTA's barrier `bar`.
+__device__ __forceinline__ void st_async_v2(uint32_t dst, uint32_t a, uint32_t b, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+          dst),
+      "r"(a), "r"(b), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t dst, uint4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
+      : "memory");
+}
+
 // generic-proxy writes to this CTA's shared memory before the fence are
 // ordered before later async-proxy accesses (tcgen05.mma operands, bulk copies)
 __device__ __forceinline__ void fence_proxy_async_cta() {

@@ -133,6 +133,31 @@ def test_quant_gemm(rf):
         assert_close_bf16(f64(y), ofp8.scaled_gemm(rq, rs, hwq.numpy(), hsw.numpy()), f"Y, replay {i}")
 
 
+@pytest.mark.parametrize("Nq", [512, 2048])
+def test_incremental_quant_gemm(rf, Nq):
+    # N = 2048 runs the cluster kernel (a cluster launch with distributed
+    # shared memory inside the graph), N = 512 the one-CTA kernel
+    Mq, Kq = 128, 768
+    x = torch.empty(Mq, Kq, dtype=torch.bfloat16, device="cuda")
+    wq = torch.empty(Nq, Kq, dtype=torch.uint8, device="cuda")
+    sw = torch.empty(Nq, device="cuda")
+    sx = torch.empty(Mq, device="cuda")
+    y = torch.empty(Mq, Nq, dtype=torch.bfloat16, device="cuda")
+    step = lambda: rf.rf_incremental_quant_fp8_gemm(x, wq, sw, y, sx)
+    for i, seed in enumerate((73, 74)):
+        hx, hwq, hsw = si.quant_gemm_inputs(Mq, Kq, Nq, seed=seed)
+        x.copy_(hx)
+        wq.copy_(hwq)
+        sw.copy_(hsw)
+        if i == 0:
+            g = capture(step)
+        replay(rf, g)
+        ry, rs = ofp8.incremental_quant_gemm(obf16.decode(hx.view(torch.int16).numpy()),
+                                             hwq.numpy(), hsw.numpy())
+        assert np.array_equal(sx.cpu().numpy(), rs), f"final scales, replay {i}"
+        assert_close_bf16(f64(y), ry, f"Y, replay {i}")
+
+
 def test_prefill(rf):
     B, H, N, D = 1, 2, 300, 128
     q = torch.empty(B, H, N, D, dtype=torch.bfloat16, device="cuda")

@@ -257,18 +257,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
   return r;
 }
 
-// Bulk copy (async proxy) of `bytes` from this CTA's shared memory to another
-// CTA of the cluster: `dst` and `bar` are shared::cluster addresses (from
-// mapa) in that CTA; the copy completes as transaction bytes on `bar`.  Both
-// addresses 16-byte aligned, `bytes` a multiple of 16.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes,
-                                                  uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Asynchronous store of 8 or 16 bytes into another CTA of the cluster (`dst`
 // and `bar` shared::cluster addresses from mapa, `dst` aligned to the size),
 // completing as transaction bytes on that CTA's barrier `bar`.

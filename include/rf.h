@@ -283,7 +283,10 @@ rf_status rf_attn_decode_noalloc(const void* q, const void* k, const void* v,
  * same rounding as rf_absmax_quant_e4m3) and accumulated on the FP8 tensor
  * cores; Y = bf16(acc * s_final * sw).  The codes of early tiles use the
  * running scale, so Y differs from rf_absmax_quant_fp8_gemm's (it is a
- * different quantisation of X, at least as fine); no Xq is written.
+ * different quantisation of X, at least as fine); no Xq is written.  When
+ * N / 512 is a multiple of 4 (8), the CTAs that share a 128-row block run as
+ * one thread-block cluster and each quantises a band of the rows for all of
+ * them; otherwise each CTA quantises its whole block.  Same results either way.
  *   x [M, K] bf16;  wq [N, K] e4m3;  sw [N] fp32;  y [M, N] bf16 out
  *   sx_final [M] fp32 out (the final per-row scale), may be NULL
  * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;

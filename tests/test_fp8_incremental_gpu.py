@@ -4,7 +4,8 @@ tolerance, the final per-row scales bit-exact.
 
 Cases: one K-tile; several tiles where the abs-max grows (outliers placed
 late, so the accumulator is rescaled); rows whose abs-max comes first (then
-the result equals the two-phase cascade's); zero rows and a zero prefix; and
+the result equals the two-phase cascade's); zero rows and a zero prefix;
+scales below 2^-90 and growth from 1e-30 to O(1) (the division paths); and
 the full workload [4096 x 7168] x [4096 x 7168] on sampled rows.  N = 512 and
 1024 run the one-CTA kernel; N = 2048 runs clusters of 4 CTAs and N = 4096
 with few rows clusters of 8 (the full workload takes clusters of 4, which
@@ -107,6 +108,29 @@ def test_zero_rows_and_zero_prefix(rf, N):
     check(rf, xf.to(torch.bfloat16), wq, sw, f"zeros N={N}")
     gy, gs = run(rf, xf.to(torch.bfloat16), wq, sw)
     assert gs[0] == 0 and np.all(gy[0] == 0)
+
+
+@pytest.mark.parametrize("N", [512, 2048])
+def test_tiny_scales(rf, N):
+    # row 0 stays near 1e-30 (scale below 2^-90: the division-per-element
+    # encoder); row 1 starts near 1e-30 and jumps to O(1) (rescale factor by
+    # the division fallback); row 2 starts at O(1e-20) and grows slowly
+    M, K = 128, 768
+    x, wq, sw = si.quant_gemm_inputs(M, K, N, seed=25)
+    xf = x.float()
+    xf[0] *= 1e-30
+    xf[1, :384] *= 1e-30
+    xf[2] *= 1e-20
+    xf[2, 700] = 3e-20
+    xb = xf.to(torch.bfloat16)
+    check(rf, xb, wq, sw, f"tiny scales N={N}")
+    # the absolute part of the bf16 tolerance says nothing about rows this
+    # small: compare them again brought up to O(1)
+    gy, gs = run(rf, xb, wq, sw)
+    ry, rs = ofp8.incremental_quant_gemm(obf16.decode(xb.view(torch.int16).numpy()), wq.numpy(),
+                                         sw.numpy())
+    for r, f in ((0, 1e30), (2, 1e20)):
+        assert_close_bf16(gy[r] * f, ry[r] * f, f"row {r} scaled by {f:g}, N={N}")
 
 
 def test_full_size_sampled_rows(rf):

@@ -238,6 +238,23 @@ def test_incremental_rescale_closed_form():
     assert y[0, 0] == 112.0 * 1.0 + 896.0 * 0.5
 
 
+def test_incremental_differs_from_two_phase():
+    """Row [1.09375, 896] in two tiles of one column, weights [1, 0]: the
+    incremental form quantises 1.09375 with its own scale s0 = fp32(1.09375 /
+    448) (code 448), so Y = 448 s0, within fp32 rounding of 1.09375; with the
+    final scale 2 throughout (the two-phase cascade) it would be coded as
+    0.546875 -> 0.5625 (the nearer e4m3 value) and Y = 1.125.  Catches an
+    incremental form that uses the final scale for every tile."""
+    x = np.array([[1.09375, 896.0]])
+    wq = np.array([[0x38, 0x00]], dtype=np.uint8)     # 1.0 and 0
+    y, s = fp8.incremental_quant_gemm(x, wq, np.ones(1, np.float32), tile_k=1)
+    assert s[0] == np.float32(2.0)
+    assert abs(y[0, 0] - 1.09375) <= 1.09375 * 2.0 ** -22
+    xq, sx = fp8.absmax_quant(x)
+    y2 = fp8.scaled_gemm(xq, sx, wq, np.ones(1, np.float32))
+    assert y2[0, 0] == 1.125
+
+
 def test_incremental_zero_prefix_and_error_bound():
     rng = np.random.default_rng(8)
     M, K, N = 4, 384, 16

@@ -38,9 +38,9 @@
 //                warp whose 32 rows did not grow skips it), and the epilogue.
 // Every barrier wait is bounded (see tc_common.cuh).  The CTAs of a cluster
 // meet at a cluster barrier before any of them exits.  A CTA that consumed
-// every tile has received every copy and commit addressed to it; one whose
+// every tile has received every store and commit addressed to it; one whose
 // waits gave up holds its shared memory a further 200 us after that barrier,
-// so that copies issued before it land in memory that is still its own.
+// so that stores issued before it land in memory that is still its own.
 
 #include <cuda_bf16.h>
 
@@ -68,7 +68,7 @@ struct Cfg {
   static constexpr int R = BM / C;            // rows this CTA converts
   static constexpr int P = CONV_THREADS / R;  // converter threads per row (2C)
   static constexpr int E = BK / P;            // columns per converter thread (64 / C)
-  static constexpr int X_BYTES = R * BK * 2;  // one bf16 band, each thread's part contiguous
+  static constexpr int X_BYTES = R * BK * 2;  // one bf16 band (chunk u of thread ct at u * 4 KiB + ct * 16)
   static constexpr int X_STAGES = C == 8 ? 4 : 3;  // tiles of X in flight per thread
 };
 
@@ -407,11 +407,11 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
 
   tc::fence_before_sync();
   __syncwarp();
-  // no CTA leaves while another may still copy into its shared memory
+  // no CTA leaves while another may still store into its shared memory
   tc::cluster_sync();
   if (warp == 1) {
     if (*abort) {
-      // copies or commits issued before the other CTAs gave up may still be
+      // stores or commits issued before the other CTAs gave up may still be
       // on their way here: hold this CTA's shared memory for 200 us
       const unsigned long long t0 = tc::globaltimer_ns();
       while (tc::globaltimer_ns() - t0 < 200000ull) {

@@ -10,8 +10,9 @@ Definitions followed:
 Readings of points the pages leave open (transcript cue 59 says the text does
 not show exactly what is fused for routing):
 
-* the k experts are the k largest probabilities; equal logits are ordered by
-  lower expert index first; the output list is sorted by that order;
+* the k experts are the k largest logits (so the k largest probabilities),
+  listed in descending order of logit; equal logits are ordered by lower
+  expert index first;
 * with ``renormalize`` the weights are the probabilities renormalised over the
   selected experts, w_i = p_i / sum_{j in sel} p_j; without it they are the
   plain probabilities p_i.
@@ -33,12 +34,17 @@ def softmax(x):
 def softmax_topk(logits, k, renormalize=True):
     """logits [T, E] -> (idx [T, k] int32, w [T, k] float64).
 
-    The ordering key is (-p, expert index): a stable sort on -p keeps equal
-    probabilities in index order.  p in float64 is strictly increasing in
-    distinct float32 logits, so ordering by p equals ordering by the logits.
+    The ordering key is (-logit, expert index), taken on the logits widened
+    exactly to float64: a stable sort on -x keeps equal logits in index
+    order (and -0 equal to +0).  The key is the logit itself, not p:
+    exp(x - m) underflows to zero (or to equal subnormals) once a logit lies
+    more than about 745 below the row maximum, and such experts must still
+    be ordered by their logits.  Where p does not underflow the two orders
+    agree, since exp is increasing.
     """
-    p = softmax(logits)
-    order = np.argsort(-p, axis=1, kind="stable")[:, :k]
+    x = np.asarray(logits, dtype=np.float64)
+    p = softmax(x)
+    order = np.argsort(-x, axis=1, kind="stable")[:, :k]
     sel = np.take_along_axis(p, order, axis=1)
     if renormalize:
         sel = sel / sel.sum(axis=1, keepdims=True)

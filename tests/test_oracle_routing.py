@@ -86,3 +86,48 @@ def test_brute_force_subsets(E):
             assert idx[t].tolist() == best
             z = sum(math.exp(row[i]) for i in best)
             np.testing.assert_allclose(w[t], [math.exp(row[i]) / z for i in best], rtol=1e-13)
+
+
+def test_order_beyond_exp_underflow():
+    # exp(x - m) is 0 in float64 for all three losers; they must still be
+    # listed by logit, not by expert index
+    x = np.array([[10.0, -900.0, -800.0, -1000.0]], dtype=np.float32)
+    idx, w = Rt.softmax_topk(x, 3, renormalize=True)
+    assert idx[0].tolist() == [0, 2, 1]
+    assert w[0].tolist() == [1.0, 0.0, 0.0]
+    idx, _ = Rt.softmax_topk(x, 4, renormalize=False)
+    assert idx[0].tolist() == [0, 2, 1, 3]
+
+
+def test_order_where_probabilities_are_equal_subnormals():
+    # gaps near 744: exp rounds the two probabilities to the same subnormal
+    # double, yet the logits differ
+    x = np.array([[0.0, -744.25, -744.0, 5.0]], dtype=np.float32)
+    m = 5.0
+    assert np.exp(np.float64(x[0, 1]) - m) == np.exp(np.float64(x[0, 2]) - m)
+    idx, _ = Rt.softmax_topk(x, 4, renormalize=False)
+    assert idx[0].tolist() == [3, 0, 2, 1]
+
+
+def test_masked_experts_with_ties():
+    # masked experts at large finite negatives, mixed with exact ties
+    x = np.array([[-1e4, 3.0, -1e4, 3.0, -3e38, -1e4, 2.0, -3e38]], dtype=np.float32)
+    idx, w = Rt.softmax_topk(x, 7, renormalize=True)
+    assert idx[0].tolist() == [1, 3, 6, 0, 2, 5, 4]
+    z = 2 * math.exp(0.0) + math.exp(-1.0)
+    np.testing.assert_allclose(w[0, :3], [1 / z, 1 / z, math.exp(-1.0) / z], rtol=1e-15)
+    assert np.all(w[0, 3:] == 0.0)
+
+
+@pytest.mark.parametrize("E", [3, 5, 8])
+def test_brute_force_subsets_with_wide_gaps(E):
+    # logits spread over +-2e4, far beyond exp's range: the best subset of
+    # size k maximises the summed logits whatever the probabilities underflow to
+    rng = np.random.default_rng(40 + E)
+    x = (rng.standard_normal((12, E)) * 1e4).astype(np.float32)
+    for k in range(1, E + 1):
+        idx, _ = Rt.softmax_topk(x, k, renormalize=False)
+        for t in range(x.shape[0]):
+            row = [float(v) for v in x[t]]
+            best = max(itertools.combinations(range(E), k), key=lambda c: sum(row[i] for i in c))
+            assert idx[t].tolist() == sorted(best, key=lambda i: (-row[i], i))

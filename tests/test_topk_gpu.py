@@ -95,3 +95,23 @@ def test_neg_inf_logits(rf):
     x[7, :] = -float("inf")
     x[7, 200] = 1.0       # one finite logit: the rest are -inf ties, lower index first
     check(rf, x, 8, True, "-inf logits")
+
+
+@pytest.mark.parametrize("E,k", [(256, 8), (64, 2), (64, 4), (128, 8), (1024, 32)])
+def test_masked_experts_far_below_the_max(rf, E, k):
+    # masked experts at large finite negatives (their probabilities underflow
+    # to zero), mixed with exact ties among the live ones and among the
+    # masked ones: the order must still follow the logits
+    T = 256
+    g = torch.Generator().manual_seed(E + k)
+    x = torch.randint(-2, 3, (T, E), generator=g).float()
+    mask = torch.rand((T, E), generator=g) < 0.6
+    fill = torch.tensor([-1e4, -3e38, -900.0, -800.0])[torch.randint(0, 4, (T, E), generator=g)]
+    x = torch.where(mask, fill, x)
+    x[3, :] = -1e4                       # every logit masked: all ties
+    x[4, :] = -3e38
+    x[4, E - 1] = -1e4                    # one survivor, the rest tied far below
+    x[5, :] = torch.where(torch.arange(E) % 2 == 0, -900.0, -800.0)
+    x[6, :k + 1] = 3.0                    # the k-th place decided by a tie among the live
+    check(rf, x, k, True, f"masked E={E} k={k}")
+    check(rf, x, k, False, f"masked E={E} k={k} no renorm")

@@ -9,10 +9,11 @@
 // synchronisation is not acceptable, or a process whose device memory budget
 // was fixed at start-up.  This entry point keeps the segment states in a
 // fixed array that is part of the library image instead, so the call itself
-// allocates nothing.  Up to kNoallocMaxRows rows it is one launch (the split
-// kernel with the merge done by each row's last CTA, counting in a second
-// fixed array of per-row counters that every completed call leaves at zero);
-// above that, the same two kernels as the regular path.
+// allocates nothing.  Every accepted call is one launch: the split kernel with
+// the merge done by each row's last CTA (as rf_attn_decode_fused), counting in
+// a second fixed array of per-row counters that every completed call leaves
+// at zero.  The size of the state array caps the rows at kNoallocMaxRows (a
+// static_assert below), so no accepted call needs more counters than that.
 //
 // Costs and rules of the shared array:
 //   * it is kRfNoallocScratchBytes (16 MiB) on every GPU that loads the
@@ -39,6 +40,12 @@ namespace {
 constexpr size_t kRfNoallocScratchBytes = 16u << 20;
 constexpr int kNoallocMaxRows = 65536;
 constexpr int kMaxDevices = 64;
+
+// The smallest request for R rows (S = 1, D = 64) needs 4*R*64 bytes of
+// accumulator states, so R rows above kNoallocMaxRows never fit: the size
+// check alone keeps every accepted call within the counters array.
+static_assert((size_t)(kNoallocMaxRows + 1) * 64 * sizeof(float) > kRfNoallocScratchBytes,
+              "the state array must cap the rows at kNoallocMaxRows");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kRfNoallocScratchBytes];
 // per-row counters of the one-launch merge: zero when the library loads, and
@@ -95,11 +102,7 @@ extern "C" rf_status rf_attn_decode_noalloc(const void* q, const void* k, const 
   float* seg_m = static_cast<float*>(base);
   float* seg_l = seg_m + states;
   float* seg_acc = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + acc_off);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (R <= rf::kNoallocMaxRows)
-    return rf::launch_decode_fused(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
-                                   counters, out, out_dtype, lse, st);
-  s = rf::launch_decode_split(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc, st);
-  if (s != RF_OK) return s;
-  return rf::launch_state_merge(seg_m, seg_l, seg_acc, R, S, D, out, out_dtype, lse, st);
+  // R <= kNoallocMaxRows here: the size check above implies it (static_assert)
+  return rf::launch_decode_fused(q, k, v, R, L, D, S, scale, dtype, seg_m, seg_l, seg_acc,
+                                 counters, out, out_dtype, lse, static_cast<cudaStream_t>(stream));
 }

@@ -25,7 +25,13 @@
  *   touched.  A failed launch returns RF_ERR_CUDA.  Nothing aborts, prints or
  *   throws across this boundary.
  * - Device pointers must be 16-byte aligned (RF_ERR_MISALIGNED otherwise).
- * - Calls are thread-safe; the library keeps no per-call global state.
+ * - Calls are thread-safe and keep no per-call state of their own, with two
+ *   exceptions: rf_attn_decode_noalloc's fixed arrays (shared by every call
+ *   on a device, see there), and the on-device status words that
+ *   rf_device_error reads.  Those words are one set per device for the whole
+ *   process: every call of every thread records into the same words, and a
+ *   read by any thread clears them for all, so one thread's rf_device_error
+ *   can consume a timeout that another thread's call recorded.
  */
 #ifndef RF_H
 #define RF_H
@@ -245,8 +251,9 @@ rf_status rf_attn_decode_fused(const void* q, const void* k, const void* v, int 
                                float* lse, void* stream);
 
 /*
- * rf_attn_decode_noalloc -- rf_attn_decode_split followed by rf_state_merge
- * for callers that cannot allocate device memory: for example a plugin inside
+ * rf_attn_decode_noalloc -- split-KV decode with the state merge in the same
+ * launch (as rf_attn_decode_fused), for callers that cannot allocate device
+ * memory: for example a plugin inside
  * a host engine that owns every device allocation, a latency-critical loop
  * that cannot afford cudaMalloc's implicit device synchronisation, or a
  * process whose memory budget was fixed at start-up.  The pages have no
@@ -256,11 +263,12 @@ rf_status rf_attn_decode_fused(const void* q, const void* k, const void* v, int 
  * out, out_dtype, lse as rf_state_merge.  The segment states live in a fixed
  * 16 MiB array inside the library (allocated once per GPU when the library
  * is loaded, kept until the process exits) instead of caller buffers, so the
- * call itself allocates nothing.  Up to 65536 rows the call is one launch,
- * as rf_attn_decode_fused, with its per-row counters in a second fixed
- * array; above that it launches the split and merge kernels.
+ * call itself allocates nothing.  Every accepted call is one launch, as
+ * rf_attn_decode_fused, with its per-row counters in a second fixed array
+ * of 65536 entries.
  * - It needs 8*R*S bytes rounded up to 256, plus 4*R*S*D bytes, to fit in
  *   16 MiB; larger requests return RF_ERR_UNSUPPORTED with nothing launched.
+ *   That limit also caps R at 65536 (even at S = 1, D = 64).
  * - Every call on a GPU shares that array: calls that may overlap on the GPU
  *   (different streams, unordered host threads) race; order them on one
  *   stream.  Each call rewrites every state it reads, so nothing needs
@@ -393,6 +401,11 @@ rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream);
  * records RF_ERR_BOUNDS.  This call synchronises `stream`, reads every such
  * word into *status (RF_OK if nothing was recorded), clears them, and
  * returns RF_OK, or RF_ERR_CUDA if the read failed.
+ * The words are process-global (one set per device, not per stream, thread
+ * or call): a status recorded by any caller's kernel is reported to whichever
+ * thread calls this first, and that read clears it for every other caller.
+ * Callers on several threads that need to attribute a status should
+ * serialise their calls and this read with a lock of their own.
  */
 rf_status rf_device_error(int* status, void* stream);
 

@@ -72,6 +72,30 @@ def test_decode_fused_validation(lib):
     assert f(*args(out=ODD)) == 3
 
 
+def test_decode_noalloc_validation(lib):
+    # every refusal below comes from the host checks, before the call looks
+    # up its static array or launches anything
+    f = lib.rf_attn_decode_noalloc
+    args = lambda **o: [o.get("q", FAKE), o.get("k", FAKE), o.get("v", FAKE), o.get("R", 4),
+                        o.get("L", 100), o.get("D", 128), o.get("S", 4), F(o.get("scale", 0.1)),
+                        o.get("dtype", 1), o.get("out", FAKE), o.get("out_dtype", 1), NULL, NULL]
+    for name in ("q", "k", "v", "out"):
+        assert f(*args(**{name: NULL})) == 1, name
+    assert f(*args(dtype=7)) == 1
+    assert f(*args(out_dtype=5)) == 1
+    assert f(*args(S=0)) == 1
+    assert f(*args(R=0)) == 1
+    assert f(*args(L=-1)) == 1
+    assert f(*args(scale=float("nan"))) == 1
+    assert f(*args(scale=float("inf"))) == 1
+    assert f(*args(D=64)) == 2              # bf16 with D=64 unsupported
+    assert f(*args(D=128, dtype=0)) == 2    # fp32 with D=128 unsupported
+    assert f(*args(R=1024, S=64)) == 2      # 34 MB of states > 16 MiB
+    assert f(*args(R=65537, S=1, D=64, dtype=0)) == 2   # the size limit caps R at 65536
+    for name in ("q", "k", "v", "out"):
+        assert f(*args(**{name: ODD})) == 3, name
+
+
 def test_decode_split_validation(lib):
     f = lib.rf_attn_decode_split
     args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, o.get("R", 4), o.get("L", 100), o.get("D", 128),

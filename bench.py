@@ -450,9 +450,19 @@ def path_routing(torch, rf, peaks, name):
     calls = [(lambda x=x: rf.rf_softmax_topk(x, k, True, idx, w)) for x in xs] * 4
     ms = time_graph(torch, calls, 10)
     gbs = nbytes / (ms * 1e-3) / 1e9
+    # the floor: one streaming read of the same logits (rf_stream_read), same
+    # copies, same graph, same timing
+    xor = torch.zeros(1, dtype=torch.int32, device="cuda")
+    reads = [(lambda x=x: rf.rf_stream_read(x, xor)) for x in xs] * 4
+    ms_floor = time_graph(torch, reads, 10)
     return {"workload": f"routing logits [{T} x {E}] fp32, top-{k}, renormalised; {copies} input "
                         f"copies rotated (> L2) in a CUDA graph",
             "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3, 2),
+            "read_floor": {"us_per_call": round(ms_floor * 1e3, 2),
+                           "GB/s": round(T * E * 4 / (ms_floor * 1e-3) / 1e9, 1),
+                           "routing_time_over_floor": round(ms / ms_floor, 3),
+                           "how": "rf_stream_read over the same input copies in the same CUDA "
+                                  "graph: one 16-byte streaming read of every logit, nothing else"},
             "roofline": roofline("hbm", gbs, peaks["hbm_gbs"], "GB/s", ncu_traffic(f"softmax_topk_{E}"))}
 
 
@@ -742,6 +752,20 @@ def run_rf(args):
     alg_bytes = kv_bytes + R * D * 2 + R * S * (D + 2) * 4
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
 
+    # the HBM read ceiling: one streaming read of K (8 GiB at full size) with
+    # the decode kernel's own 16-byte loads and nothing else
+    xor = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        rf.rf_stream_read(K, xor, stream)
+    n_read = 5
+    ra, rb = _events(torch, 2)
+    ra.record(stream)
+    for _ in range(n_read):
+        rf.rf_stream_read(K, xor, stream)
+    rb.record(stream)
+    torch.cuda.synchronize()
+    read_ceiling = K.numel() * K.element_size() / (ra.elapsed_time(rb) / n_read * 1e-3) / 1e9
+
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -837,7 +861,12 @@ def run_rf(args):
                                  ncu_traffic("decode_split")),
             "roofline_kernel": {"name": "decode_split_kernel", "avg_ms": round(kern_ms, 4),
                                 "alg_bytes_per_launch": alg_bytes,
-                                "peak_source": f"{peaks['source']} hbm_gbs (burst copy)"},
+                                "peak_source": f"{peaks['source']} hbm_gbs (burst copy)",
+                                "frac_of_read_ceiling": round(achieved / read_ceiling, 4)},
+            "read_ceiling_gbs": round(read_ceiling, 1),
+            "read_ceiling_how": (f"rf_stream_read over K ({K.numel() * K.element_size()} bytes): "
+                                 f"one 16-byte streaming read of every byte, the decode kernel's "
+                                 f"load, nothing else; mean of {n_read} calls"),
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,
             "clocks": clk,

@@ -58,6 +58,7 @@ _SIGNATURES = {
     "rf_attn_decode_fused": (_I, [_P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _I, _P, _P]),
     "rf_bounds_checked": (_I, []),
     "rf_selftest_bounds": (_I, [_P]),
+    "rf_stream_read": (_I, [_P, ctypes.c_size_t, _P, _P]),
 }
 
 
@@ -354,6 +355,16 @@ def rf_incremental_quant_fp8_gemm(x, wq, sw, y, sx_final=None, stream=None):
     _check(_lib.rf_incremental_quant_fp8_gemm(_ptr(x), M, K, _ptr(wq), _ptr(sw), N, _ptr(y),
                                               _ptr(sx_final), _stream(stream)),
            "rf_incremental_quant_fp8_gemm")
+
+
+def rf_stream_read(x, out_xor, stream=None):
+    """XOR every 32-bit word of the CUDA tensor ``x`` into ``out_xor`` (one
+    int32 element, device memory) with one streaming read of ``x``."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    _need(out_xor, torch.int32, "out_xor", (1,))
+    _check(_lib.rf_stream_read(_ptr(x), x.numel() * x.element_size(), _ptr(out_xor),
+                               _stream(stream)), "rf_stream_read")
 
 
 def rf_selftest_wait_timeout(waited_ms, stream=None):

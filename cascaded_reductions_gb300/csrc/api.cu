@@ -113,7 +113,7 @@ rf_status rf_softmax_topk(const float* logits, int T, int E, int k, int renormal
   if (!logits || !idx || !w) return RF_ERR_INVALID_ARG;
   if (T <= 0 || E <= 0 || k < 1 || k > E) return RF_ERR_INVALID_ARG;
   if (E > 1024 || k > 32) return RF_ERR_UNSUPPORTED;
-  if (!rf::aligned16(logits)) return RF_ERR_MISALIGNED;
+  if (!rf::aligned16(logits) || !rf::aligned16(idx) || !rf::aligned16(w)) return RF_ERR_MISALIGNED;
   return rf::launch_softmax_topk(logits, T, E, k, renormalize ? 1 : 0, idx, w, as_stream(stream));
 }
 

@@ -185,6 +185,7 @@ rf_status launch_rms_norm(const float* x, const float* gamma, int R, int n, floa
                           int level, float* work, cudaStream_t st);
 rf_status launch_mla_decode(const void* q, const void* c, int B, int H, int L, int S, float scale,
                             float* seg_m, float* seg_l, float* seg_acc, cudaStream_t st);
+rf_status launch_stream_read(const void* x, size_t nbytes, uint32_t* out_xor, cudaStream_t st);
 rf_status launch_selftest_wait_timeout(int* waited_ms, cudaStream_t st);
 rf_status launch_selftest_bounds(cudaStream_t st);
 rf_status read_device_error(int* status, cudaStream_t st);

@@ -5,8 +5,10 @@
 // exp-sum denominator and the k largest entries all come from a single pass
 // over the logits held in registers.
 //
-// Two kernels.  For E <= 128 (with k <= G), softmax_topk_merge_kernel: each
-// lane keeps its best two logits and the group merges lane heads round by
+// Three kernels.  For k <= 2 and E a multiple of 32 up to 128,
+// softmax_top2_row_kernel: one thread per token over a row staged in shared
+// memory (below).  For other E <= 128 (with k <= G), softmax_topk_merge_kernel:
+// each lane keeps its best two logits and the group merges lane heads round by
 // round (below).  Otherwise softmax_topk_kernel:
 //
 // Layout: a group of G lanes (G = 8, 16 or 32) owns TPG tokens, one after the
@@ -406,6 +408,144 @@ softmax_topk_merge_kernel(const float* __restrict__ logits, int T, int E, int k_
   }
 }
 
+// One thread per token, for k <= 2 and E a multiple of 32 (up to 128).
+//
+// A block of TPB threads stages its TPB rows in shared memory with 16-byte
+// cp.async copies, coalesced across the block, in two commit groups: the
+// first half of every row's chunks, then the second half.  Chunk c of row r
+// lands at position c ^ (r & 7) of the row, so when the 32 threads of a warp
+// each read the same chunk of their own rows, every 8-thread phase of the
+// 16-byte loads touches 8 different bank groups.  Each thread scans its row
+// in expert order with NCH independent top-2 chains (chunk c belongs to chain
+// c % NCH, so the chains' compares overlap), the first half while the second
+// half is still landing, and merges the chains under the same order: larger
+// value first, equal values by lower expert index.  Per token this is a few
+// dozen thread instructions, about one warp instruction per element of 32
+// tokens, against a few hundred warp instructions per token in the warp-wide
+// selection.  Measured at [65536 x 64]: the staging alone runs at the read
+// floor, and the second commit group hides half of the scan behind the
+// stream.  The weights need only the best two: with renormalisation
+// w1 = 1 / (1 + e), w2 = e / (1 + e), e = exp(x2 - x1); without it a second
+// pass over the staged row sums exp(x - x1).
+template <int E, int TPB, int NCH>
+__global__ void __launch_bounds__(TPB)
+softmax_top2_row_kernel(const float* __restrict__ logits, int T, int k, int renorm,
+                        int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+  constexpr int CH = E / 4;                       // 16-byte chunks per row
+  constexpr int HALF = CH / 2;
+  static_assert(E % 32 == 0 && HALF % NCH == 0, "rows of whole 8-chunk swizzle groups");
+  __shared__ __align__(16) float4 rows[TPB * CH];
+  const int t0 = blockIdx.x * TPB;
+  const int nrows = min(TPB, T - t0);
+  const float4* src = reinterpret_cast<const float4*>(logits) + (size_t)t0 * CH;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    for (int q = threadIdx.x; q < nrows * HALF; q += TPB) {
+      const int r = q / HALF, c = h * HALF + q % HALF;
+      if (RF_SPAN_OK(((size_t)t0 * CH + (size_t)r * CH + c) * 4, 4, (long long)T * E)) {
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&rows[r * CH + (c ^ (r & 7))]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + r * CH + c)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+  __syncthreads();
+  // threads past the last row stay for the second barrier, then leave
+  const int r = threadIdx.x < nrows ? threadIdx.x : nrows - 1;
+  const float4* row = rows + r * CH;
+  const int sw = r & 7;
+  float v1[NCH], v2[NCH];
+  int s1[NCH], s2[NCH];
+  // strict compares keep the lower expert first among equal values, because
+  // each chain visits its experts in increasing order
+  auto fold = [&](int p, float x, int i) {
+    const bool c1 = x > v1[p], c2 = x > v2[p];
+    v2[p] = c1 ? v1[p] : (c2 ? x : v2[p]);
+    s2[p] = c1 ? s1[p] : (c2 ? i : s2[p]);
+    v1[p] = c1 ? x : v1[p];
+    s1[p] = c1 ? i : s1[p];
+  };
+  // chain p starts from chunk p: its first two values in order, then the rest
+#pragma unroll
+  for (int p = 0; p < NCH; ++p) {
+    const float4 f = row[p ^ sw];
+    const int b = 4 * p;
+    const bool up = f.y > f.x;
+    v1[p] = up ? f.y : f.x;
+    s1[p] = up ? b + 1 : b;
+    v2[p] = up ? f.x : f.y;
+    s2[p] = up ? b : b + 1;
+    fold(p, f.z, b + 2);
+    fold(p, f.w, b + 3);
+  }
+#pragma unroll
+  for (int j = 1; j < CH / NCH; ++j) {
+    if (j == HALF / NCH) {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();
+    }
+#pragma unroll
+    for (int p = 0; p < NCH; ++p) {
+      const int c = NCH * j + p;
+      const float4 f = row[c ^ sw];
+      fold(p, f.x, 4 * c);
+      fold(p, f.y, 4 * c + 1);
+      fold(p, f.z, 4 * c + 2);
+      fold(p, f.w, 4 * c + 3);
+    }
+  }
+  if (threadIdx.x >= nrows) return;
+  // merge the chains: (a, ia) ranks above (b, ib) if a > b, or a == b and ia < ib
+  auto above = [](float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); };
+  float x1 = v1[0], x2 = v2[0];
+  int i1 = s1[0], i2 = s2[0];
+#pragma unroll
+  for (int p = 1; p < NCH; ++p) {
+    const bool c = above(v1[p], s1[p], x1, i1);
+    const float a = c ? x1 : x2, b = c ? v2[p] : v1[p];
+    const int ia = c ? i1 : i2, ib = c ? s2[p] : s1[p];
+    const bool d = above(b, ib, a, ia);
+    x1 = c ? v1[p] : x1;
+    i1 = c ? s1[p] : i1;
+    x2 = d ? b : a;
+    i2 = d ? ib : ia;
+  }
+  const float e2 = __expf(x2 - x1);             // weight of the second, relative to the first
+  float denom;
+  if (renorm) {
+    denom = k == 2 ? 1.f + e2 : 1.f;
+  } else {
+    float l = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const float4 f = row[c ^ sw];
+      l += __expf(f.x - x1) + __expf(f.y - x1) + __expf(f.z - x1) + __expf(f.w - x1);
+    }
+    denom = l;
+  }
+  const size_t token = (size_t)(t0 + r);
+  if (k == 2) {
+    if (RF_SPAN_OK(token * 2, 2, (long long)T * 2)) {
+      reinterpret_cast<int2*>(idx_out)[token] = make_int2(i1, i2);
+      reinterpret_cast<float2*>(w_out)[token] =
+          make_float2(__fdividef(1.f, denom), __fdividef(e2, denom));
+    }
+  } else if (RF_IDX_OK(token, T)) {
+    idx_out[token] = i1;
+    w_out[token] = __fdividef(1.f, denom);
+  }
+}
+
+template <int E>
+void launch_top2_rows(const float* logits, int T, int k, int renorm, int32_t* idx, float* w,
+                      cudaStream_t st) {
+  constexpr int TPB = 64;      // measured at E = 64: 64 and 128 alike, 32 slower
+  const unsigned grid = (unsigned)((T + TPB - 1) / TPB);
+  softmax_top2_row_kernel<E, TPB, 2><<<grid, TPB, 0, st>>>(logits, T, k, renorm, idx, w);
+}
+
 constexpr int kMergeBlocksPerSm = 8;     // measured best of 2, 4, 8, 16 at [65536 x 64]
 
 template <int G, int NV, int W>
@@ -444,6 +584,15 @@ void launch_one(const float* logits, int T, int E, int k, int renorm, int32_t* i
 rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int renormalize,
                               int32_t* idx, float* w, cudaStream_t st) {
   const bool v4 = E % 4 == 0;
+  if (k <= 2 && E % 32 == 0 && E <= 128) {
+    switch (E) {
+      case 32: launch_top2_rows<32>(logits, T, k, renormalize, idx, w, st); break;
+      case 64: launch_top2_rows<64>(logits, T, k, renormalize, idx, w, st); break;
+      case 96: launch_top2_rows<96>(logits, T, k, renormalize, idx, w, st); break;
+      default: launch_top2_rows<128>(logits, T, k, renormalize, idx, w, st); break;
+    }
+    return launch_status();
+  }
   // lanes r < k of a group keep round r's winner, so G >= k
   if (E <= 64 && k <= 4) {
     if (v4) launch_merge<4, 16, 4>(logits, T, E, k, renormalize, idx, w, st);

@@ -36,6 +36,7 @@
 #ifndef RF_H
 #define RF_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -194,7 +195,8 @@ rf_status rf_attn_prefill(const void* q, const void* k, const void* v,
  *                              equal logits by lower index first
  *   w       [T, k]  fp32 out   routing weights in the same order
  * Errors: RF_ERR_INVALID_ARG for null pointers, T, E <= 0, k < 1 or k > E;
- * RF_ERR_UNSUPPORTED for E > 1024 or k > 32.
+ * RF_ERR_UNSUPPORTED for E > 1024 or k > 32; RF_ERR_MISALIGNED unless
+ * logits, idx and w are 16-byte aligned.
  */
 rf_status rf_softmax_topk(const float* logits, int T, int E, int k, int renormalize,
                           int32_t* idx, float* w, void* stream);
@@ -389,6 +391,22 @@ rf_status rf_rms_norm(const float* x, const float* gamma, int R, int n, float ep
  * reported by the next rf_device_error call, not by this call.
  */
 rf_status rf_selftest_wait_timeout(int* waited_ms, void* stream);
+
+/*
+ * rf_stream_read -- the read-bandwidth probe.  The pages have no counterpart:
+ * it is the measuring stick for the HBM-bound calls above.  It reads
+ * nbytes of x once, with the 16-byte non-coherent streaming loads the
+ * decode and routing kernels use, and XORs every 32-bit word of x into
+ * *out_xor (so *out_xor ^= w_0 ^ w_1 ^ ...; zero it first for the plain
+ * checksum).  Timed over a cascade's own input it gives that cascade's
+ * floor; timed over gigabytes it gives the HBM read ceiling.
+ *   x        device memory, nbytes long, 16-byte aligned
+ *   out_xor  [1] uint32, device memory, in/out
+ * Errors: RF_ERR_INVALID_ARG for null pointers or nbytes == 0;
+ * RF_ERR_UNSUPPORTED unless nbytes % 16 == 0; RF_ERR_MISALIGNED unless x is
+ * 16-byte and out_xor 4-byte aligned.
+ */
+rf_status rf_stream_read(const void* x, size_t nbytes, uint32_t* out_xor, void* stream);
 
 /*
  * rf_device_error -- status of the on-device checks.  The tensor-core

@@ -130,14 +130,29 @@ def test_merge_validation(lib):
 def test_topk_validation(lib):
     f = lib.rf_softmax_topk
     args = lambda **o: [o.get("x", FAKE), o.get("T", 10), o.get("E", 64), o.get("k", 2), 1,
-                        FAKE, FAKE, NULL]
+                        o.get("idx", FAKE), o.get("w", FAKE), NULL]
     assert f(*args(x=NULL)) == 1
+    assert f(*args(idx=NULL)) == 1
+    assert f(*args(w=NULL)) == 1
     assert f(*args(T=0)) == 1
     assert f(*args(k=0)) == 1
     assert f(*args(k=65)) == 1            # k > E
     assert f(*args(E=2048, k=4)) == 2
     assert f(*args(E=100, k=40)) == 2     # k > 32
     assert f(*args(x=ODD)) == 3
+    assert f(*args(idx=ODD)) == 3
+    assert f(*args(w=ODD)) == 3
+
+
+def test_stream_read_validation(lib):
+    f = lib.rf_stream_read
+    f.argtypes = [P, ctypes.c_size_t, P, P]
+    assert f(NULL, 64, FAKE, NULL) == 1
+    assert f(FAKE, 64, NULL, NULL) == 1
+    assert f(FAKE, 0, FAKE, NULL) == 1
+    assert f(FAKE, 40, FAKE, NULL) == 2     # not a multiple of 16 bytes
+    assert f(ODD, 64, FAKE, NULL) == 3
+    assert f(FAKE, 64, P(0x10002), NULL) == 3
 
 
 def test_quant_gemm_validation(lib):

@@ -115,3 +115,32 @@ def test_masked_experts_far_below_the_max(rf, E, k):
     x[6, :k + 1] = 3.0                    # the k-th place decided by a tie among the live
     check(rf, x, k, True, f"masked E={E} k={k}")
     check(rf, x, k, False, f"masked E={E} k={k} no renorm")
+
+
+@pytest.mark.parametrize("E", [32, 64, 96, 128])
+@pytest.mark.parametrize("k", [1, 2])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 1000])
+def test_one_thread_per_token_shapes(rf, E, k, T):
+    # k <= 2 with E a multiple of 32 up to 128: one thread per token over a
+    # row staged in shared memory; T around the 64-token block (ragged tails)
+    x = si.routing_logits(T, E, seed=1000 * E + 10 * k + T)
+    check(rf, x, k, True, f"E={E} k={k} T={T}")
+    check(rf, x, k, False, f"E={E} k={k} T={T} no renorm")
+
+
+@pytest.mark.parametrize("E", [32, 64, 128])
+def test_one_thread_per_token_ties_and_order(rf, E):
+    T = 200
+    g = torch.Generator().manual_seed(E)
+    x = torch.randint(-2, 3, (T, E), generator=g).float()   # ties everywhere
+    x[0, :] = 1.0                                          # all tied: experts 0, 1
+    x[1, :] = -1e4
+    x[1, E - 1] = 5.0
+    x[1, E - 2] = 5.0                                      # the two best tie at the end
+    x[2, :] = torch.arange(E, dtype=torch.float32)         # increasing: E-1, E-2
+    x[3, :] = -torch.arange(E, dtype=torch.float32)        # decreasing: 0, 1
+    x[4, :] = 0.0
+    x[4, 5] = -0.0                                         # -0 ties with +0
+    for k in (1, 2):
+        check(rf, x, k, True, f"ties E={E} k={k}")
+        check(rf, x, k, False, f"ties E={E} k={k} no renorm")

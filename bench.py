@@ -764,7 +764,8 @@ def run_rf(args):
         rf.rf_stream_read(K, xor, stream)
     rb.record(stream)
     torch.cuda.synchronize()
-    read_ceiling = K.numel() * K.element_size() / (ra.elapsed_time(rb) / n_read * 1e-3) / 1e9
+    k_bytes = K.numel() * K.element_size()
+    read_ceiling = k_bytes / (ra.elapsed_time(rb) / n_read * 1e-3) / 1e9
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -864,7 +865,7 @@ def run_rf(args):
                                 "peak_source": f"{peaks['source']} hbm_gbs (burst copy)",
                                 "frac_of_read_ceiling": round(achieved / read_ceiling, 4)},
             "read_ceiling_gbs": round(read_ceiling, 1),
-            "read_ceiling_how": (f"rf_stream_read over K ({K.numel() * K.element_size()} bytes): "
+            "read_ceiling_how": (f"rf_stream_read over K ({k_bytes} bytes): "
                                  f"one 16-byte streaming read of every byte, the decode kernel's "
                                  f"load, nothing else; mean of {n_read} calls"),
             "e2e": e2e,

@@ -134,7 +134,14 @@ def test_tiny_scales(rf, N):
 
 
 def test_full_size_sampled_rows(rf):
+    # 256 rows of the full workload: two whole 128-row blocks (the first and
+    # the last; every row of a block is quantised by the cluster that shares
+    # it) and 64 rows drawn across the rest
     cfg = si.FULL["quant_gemm"]
-    x, wq, sw = si.quant_gemm_inputs(cfg["M"], cfg["K"], cfg["N"], seed=si.SEEDS["quant_gemm"])
-    rows = sorted(set(np.random.default_rng(0).choice(cfg["M"], 48, replace=False).tolist() + [0, 4095]))
+    M = cfg["M"]
+    x, wq, sw = si.quant_gemm_inputs(M, cfg["K"], cfg["N"], seed=si.SEEDS["quant_gemm"])
+    rows = set(range(0, 128)) | set(range(M - 128, M))
+    rows |= set(np.random.default_rng(0).choice(np.arange(128, M - 128), 64, replace=False).tolist())
+    rows = sorted(rows)
+    assert len(rows) >= 256
     check(rf, x, wq, sw, "4096x7168x4096", rows=rows)

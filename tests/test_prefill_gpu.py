@@ -91,3 +91,10 @@ def test_full_size_sampled_rows(rf):
                                         scale, i)
         assert_close_bf16(f64(out[b, h, i]), ro, f"out ({b},{h},{i})")
         assert_close_f32(np.array([f64(lse[b, h, i])]), np.array([rl]), f"lse ({b},{h},{i})")
+    # two whole heads, every one of their 8192 rows element by element: the
+    # first head (computed first in the launch's heavy-first pair order) and
+    # the last
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        ro, rl = A.causal_attention(f64(q[b, h]), f64(k[b, h]), f64(v[b, h]), scale, causal=True)
+        assert_close_bf16(f64(out[b, h]), ro, f"out head ({b},{h})")
+        assert_close_f32(f64(lse[b, h]), rl, f"lse head ({b},{h})")

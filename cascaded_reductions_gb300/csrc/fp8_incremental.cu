@@ -233,8 +233,8 @@ fp8_incremental_kernel(const __grid_constant__ CUtensorMap tmX,
         if (s_cur == 0.f) {
           lo = hi = make_uint2(0u, 0u);
         } else if (fast_scale(s_cur)) {
-          lo = encode8(xv[2 * j], s_cur, rcp);
-          hi = encode8(xv[2 * j + 1], s_cur, rcp);
+          lo = encode8_x2(xv[2 * j], s_cur, rcp);
+          hi = encode8_x2(xv[2 * j + 1], s_cur, rcp);
         } else {
           lo = encode8_exact(xv[2 * j], s_cur);
           hi = encode8_exact(xv[2 * j + 1], s_cur);

@@ -110,7 +110,7 @@ __device__ __forceinline__ void encode_row_part(const uint4 (&xv)[E / 8], float 
     if (s == 0.f)
       codes[u] = make_uint2(0u, 0u);
     else if (fast_scale(s))
-      codes[u] = encode8(xv[u], s, rcp);
+      codes[u] = encode8_x2(xv[u], s, rcp);
     else
       codes[u] = encode8_exact(xv[u], s);
   }

@@ -20,14 +20,14 @@
 //               in shared memory; O += P V reads P from TMEM (the softmax
 //               writes it as bf16 pairs over the first 64 columns of S) and V
 //               MN-major from shared memory;
-//   warps 0-7   softmax of tile A, warps 8-15 softmax of tile B: two threads
-//               per query row (TMEM lane), one per 64-key half.  A thread
-//               loads its 64 scores, the halves exchange partial row maxima
-//               through shared memory (an mbarrier per tile, row quarter and
-//               step, bounded like every other wait), then each thread
-//               exponentiates its keys in the log2 domain (scores times
-//               scale*log2(e)), writes its half of P, and rescales its half
-//               of O when needed.
+//   warps 0-7   softmax of tile A, warps 8-15 softmax of tile B: each warp
+//               reads 16 query rows (TMEM lanes) of S with the 16x256b shape,
+//               which gives every thread 32 keys of two rows and puts the
+//               four threads of a row in adjacent lanes: the row max is two
+//               xor shuffles.  Each thread exponentiates its keys in the log2
+//               domain (scores times scale*log2(e)), writes its bf16 pairs of
+//               P with the matching 16x128b store, and rescales its part of O
+//               when needed.
 // Rescaling is lazy: the reference max m_ref of a row moves (and O and l are
 // multiplied by exp2(m_ref_old - m_ref_new)) only when the tile max exceeds
 // it by more than 8, so p <= 2^8.  The result is the same mathematics (O and
@@ -63,10 +63,9 @@ struct Shared {
   uint64_t s_full[2];          // per tile
   uint64_t p_ready[2];         // per tile, 8 softmax warps
   uint64_t o_done[2];          // per tile
-  uint64_t max_ready[2][4];    // per tile and row quarter (2 warps), one phase per step
   uint64_t l_ready[2];         // per tile, 8 softmax warps
-  float pmax[2][2][2][BM];     // [tile][step parity][half][row]
-  float l_part[2][2][BM];      // [tile][half][row]
+  float row_l[2][BM];          // [tile][row]: the row's sum, for the epilogue
+  float row_m[2][BM];          // [tile][row]: the row's reference max (log2 units)
   uint32_t tmem_base;
   int abort;
 };
@@ -181,8 +180,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       tc::mbar_init(&sh->s_full[x], 1);
       tc::mbar_init(&sh->p_ready[x], 8);
       tc::mbar_init(&sh->o_done[x], 1);
-      for (int q4 = 0; q4 < 4; ++q4)
-        tc::mbar_init(&sh->max_ready[x][q4], 2);
       tc::mbar_init(&sh->l_ready[x], 8);
     }
     sh->abort = 0;
@@ -263,92 +260,106 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
     }
   } else {
     // --------------------------------------------------- softmax ----
+    // Warp (quarter, sub) of a tile owns TMEM lanes 32 quarter + 16 sub ..
+    // + 15 and reads them with the 16x256b shape: thread t holds rows
+    // r0 = t / 4 and r0 + 8 of those 16, keys 8k + 2 (t % 4) + {0, 1} for
+    // k = 0..15.  The four threads of a row are adjacent lanes, so its max is
+    // two xor shuffles.
     const int x = warp >> 3;                        // tile A (0) or B (1)
-    const int quarter = warp & 3, half = (warp >> 2) & 1;
-    const int r = quarter * 32 + lane;              // query row in the tile (TMEM lane)
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int col0 = half * 64;
+    const int quarter = warp & 3, sub = (warp >> 2) & 1;
+    const int cq = lane & 3;                        // key pair within each group of 8 keys
+    const int r0 = quarter * 32 + sub * 16 + (lane >> 2);   // rows r0 and r0 + 8 of the tile
+    const uint32_t lane16 = tmem + ((uint32_t)(quarter * 32 + sub * 16) << 16);
     const int n = x ? nblk1 : nblk0;
     const int m_tile = x ? m_tile1 : m_tile0;
-    float m_ref = -INFINITY, l = 0.f;
+    float m_ref[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
     bool ok = n > 0;
+    const uint64_t sl2 = pack_f32x2(scale_log2, scale_log2);
     for (int j = 0; j < n && ok; ++j) {
       if (!tc::mbar_wait(&sh->s_full[x], (uint32_t)j & 1u, abort)) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      float s[64];
+      float s[2][32];                               // s[row][2k + e] = key 8k + 2 cq + e
       {
-        uint32_t v0[32], v1[32];
-        const uint32_t sb = lane_base + s_col(x) + (uint32_t)col0;
-        tc::tmem_ld_32x32b_x32(sb, v0);
-        tc::tmem_ld_32x32b_x32(sb + 32u, v1);
+        uint32_t v[64];
+        tc::tmem_ld_16x256b_x16(lane16 + s_col(x), v);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(v0[i]);
-          s[32 + i] = __uint_as_float(v1[i]);
+        for (int k = 0; k < 16; ++k) {
+          s[0][2 * k] = __uint_as_float(v[4 * k]);
+          s[0][2 * k + 1] = __uint_as_float(v[4 * k + 1]);
+          s[1][2 * k] = __uint_as_float(v[4 * k + 2]);
+          s[1][2 * k + 1] = __uint_as_float(v[4 * k + 3]);
         }
       }
       if (causal && j == m_tile) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (col0 + i > r) s[i] = -INFINITY;
+        for (int k = 0; k < 16; ++k)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = 8 * k + 2 * cq + e;
+            if (key > r0) s[0][2 * k + e] = -INFINITY;
+            if (key > r0 + 8) s[1][2 * k + e] = -INFINITY;
+          }
       } else if (!causal && j == NB - 1 && N % BN != 0) {
         // keys past N in the last tile are the next head's rows (or TMA's
         // zero fill): leave them out.  Under the causal mask they never count
         // for a row that is stored.
         const int kmax = N - j * BN;
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (col0 + i >= kmax) s[i] = -INFINITY;
-      }
-      // partial max of this half (raw scores; scale_log2 > 0 is applied
-      // later), three-input max: half the instructions of a two-input chain
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int k = 0; k < 16; ++k)
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], s[i], s[i + 1]);
-      const float pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      // exchange with the other half of the row
-      sh->pmax[x][j & 1][half][r] = pm;
-      __syncwarp();
-      // the two warps that share this row quarter
-      if (lane == 0) tc::mbar_arrive(&sh->max_ready[x][quarter]);
-      if (!tc::mbar_wait(&sh->max_ready[x][quarter], (uint32_t)j & 1u, abort)) {
-        ok = false;
-        break;
+          for (int e = 0; e < 2; ++e)
+            if (8 * k + 2 * cq + e >= kmax) {
+              s[0][2 * k + e] = -INFINITY;
+              s[1][2 * k + e] = -INFINITY;
+            }
       }
-      const float mt = fmaxf(pm, sh->pmax[x][j & 1][half ^ 1][r]) * scale_log2;
-      // move the reference max only when it has grown by more than the threshold
-      const bool move = mt > m_ref + RESCALE_THRESHOLD;
-      const float m_new = move ? mt : m_ref;
-      const float alpha = ex2(m_ref - m_new);       // 0 on the first tile, 1 when not moved
-      l *= alpha;
-      // this thread's 64 keys of P into its 32 columns of S (two bf16 per column)
-      // arguments and row sums on pairs of keys (packed fp32x2 FMA and add)
-      uint64_t sum2[2] = {0ull, 0ull};
-      const uint64_t sl2 = pack_f32x2(scale_log2, scale_log2);
-      const uint64_t nm2 = pack_f32x2(-m_new, -m_new);
+      float m_new[2], alpha[2];
+      bool move_any = false;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[16];
+      for (int h = 0; h < 2; ++h) {
+        // row max over this thread's 32 keys (three-input max), then over the
+        // row's four threads; raw scores (scale_log2 > 0 is applied after)
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t a = fma_f32x2(pack_f32x2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2, nm2);
-          const float p0 = ex2(lo_f32(a));
-          const float p1 = ex2(hi_f32(a));
-          const uint64_t p = pack_f32x2(p0, p1);
-          sum2[i & 1] = add_f32x2(sum2[i & 1], p);
-          w[i] = pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st_32x32b_x16(lane_base + s_col(x) + (uint32_t)(half * 32 + c * 16), w);
+        for (int i = 0; i < 32; i += 2) mx[(i >> 1) & 3] = max3(mx[(i >> 1) & 3], s[h][i], s[h][i + 1]);
+        float pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+        const float mt = pm * scale_log2;
+        // move the reference max only when it has grown by more than the threshold
+        const bool move = mt > m_ref[h] + RESCALE_THRESHOLD;
+        m_new[h] = move ? mt : m_ref[h];
+        alpha[h] = ex2(m_ref[h] - m_new[h]);        // 0 on the first tile, 1 when not moved
+        l[h] *= alpha[h];
+        m_ref[h] = m_new[h];
+        move_any |= move;
       }
+      // P = exp2(s * scale_log2 - m) as bf16 pairs over the first 64 columns
+      // of S (key pair (8k + 2 cq, + 1) -> column 4k + cq), row sums on pairs
+      // (packed fp32x2 FMA and add)
       {
-        const uint64_t t2 = add_f32x2(sum2[0], sum2[1]);
-        l += lo_f32(t2) + hi_f32(t2);
+        uint32_t w[32];
+        uint64_t sum2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint64_t nm2 = pack_f32x2(-m_new[h], -m_new[h]);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint64_t a = fma_f32x2(pack_f32x2(s[h][2 * k], s[h][2 * k + 1]), sl2, nm2);
+            const float p0 = ex2(lo_f32(a));
+            const float p1 = ex2(hi_f32(a));
+            sum2[h] = add_f32x2(sum2[h], pack_f32x2(p0, p1));
+            w[2 * k + h] = pack_bf16x2(p0, p1);
+          }
+        }
+        tc::tmem_st_16x128b_x16(lane16 + s_col(x), w);
+        l[0] += lo_f32(sum2[0]) + hi_f32(sum2[0]);
+        l[1] += lo_f32(sum2[1]) + hi_f32(sum2[1]);
       }
-      m_ref = m_new;
       // O must hold every earlier P V before it is rescaled
       if (j > 0) {
         if (!tc::mbar_wait(&sh->o_done[x], (uint32_t)(j - 1) & 1u, abort)) {
@@ -356,21 +367,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
           break;
         }
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, move)) {
+        if (__any_sync(0xffffffffu, move_any)) {
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
-            const uint32_t oc = lane_base + o_col(x) + (uint32_t)(col0 + c * 32);
+            const uint32_t oc = lane16 + o_col(x) + (uint32_t)(c * 64);
             uint32_t v[32];
-            tc::tmem_ld_32x32b_x32(oc, v);
+            tc::tmem_ld_16x256b_x8(oc, v);
             tc::tmem_ld_wait();
-            uint32_t w0[16], w1[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              w0[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-              w1[i] = __float_as_uint(__uint_as_float(v[16 + i]) * alpha);
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] = __float_as_uint(__uint_as_float(v[4 * k]) * alpha[0]);
+              v[4 * k + 1] = __float_as_uint(__uint_as_float(v[4 * k + 1]) * alpha[0]);
+              v[4 * k + 2] = __float_as_uint(__uint_as_float(v[4 * k + 2]) * alpha[1]);
+              v[4 * k + 3] = __float_as_uint(__uint_as_float(v[4 * k + 3]) * alpha[1]);
             }
-            tc::tmem_st_32x32b_x16(oc, w0);
-            tc::tmem_st_32x32b_x16(oc + 16u, w1);
+            tc::tmem_st_16x256b_x8(oc, v);
           }
         }
       }
@@ -380,15 +391,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       if (lane == 0) tc::mbar_arrive(&sh->p_ready[x]);
     }
     if (n > 0) {
-      // the two halves of each row add their partial sums
-      sh->l_part[x][half][r] = l;
+      // each row's sum over its four threads; one thread per row publishes
+      // the row's sum and reference for the epilogue
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 1);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 2);
+      }
+      if (cq == 0) {
+        sh->row_l[x][r0] = l[0];
+        sh->row_l[x][r0 + 8] = l[1];
+        sh->row_m[x][r0] = m_ref[0];
+        sh->row_m[x][r0 + 8] = m_ref[1];
+      }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->l_ready[x]);
-      // epilogue: out = O / l, lse = (m_ref + log2 l) * ln 2
+      // epilogue, one thread per row (32x32b shape): warp (quarter, sub)
+      // writes columns 64 sub .. 64 sub + 63 of rows 32 quarter .. + 31.
+      // out = O / l, lse = (m_ref + log2 l) * ln 2
       if (ok && tc::mbar_wait(&sh->l_ready[x], 0, abort) &&
           tc::mbar_wait(&sh->o_done[x], (uint32_t)(n - 1) & 1u, abort)) {
         tc::fence_after_sync();
-        const float lt = sh->l_part[x][0][r] + sh->l_part[x][1][r];
+        const int r = quarter * 32 + lane;
+        const int col0 = sub * 64;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float lt = sh->row_l[x][r];
         const float inv = 1.f / lt;
         const int grow = key0 + m_tile * BM + r;      // global query row
         const bool row_in = m_tile * BM + r < N;      // rows past N belong to no query
@@ -412,9 +439,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
               dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
           }
         }
-        if (lse != nullptr && half == 0 && row_in &&
+        if (lse != nullptr && sub == 0 && row_in &&
             RF_IDX_OK(grow, (long long)(gridDim.x / NP) * N))
-          lse[grow] = (m_ref + log2f(lt)) * kLn2;
+          lse[grow] = (sh->row_m[x][r] + log2f(lt)) * kLn2;
       }
     }
   }

@@ -81,7 +81,7 @@ absmax_quant_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict__ xq,
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int c = i * THREADS + threadIdx.x;
-      if (c < K8 && RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8(v[i], s, r);
+      if (c < K8 && RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8_x2(v[i], s, r);
     }
   } else {
 #pragma unroll 1
@@ -108,7 +108,7 @@ absmax_quant_long_kernel(const uint4* __restrict__ x, int K8, uint2* __restrict_
   if (fast_scale(s)) {
     const float r = __frcp_rn(s);
     for (int c = threadIdx.x; c < K8; c += THREADS)
-      if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8(x[base + c], s, r);
+      if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8_x2(x[base + c], s, r);
   } else {
     for (int c = threadIdx.x; c < K8; c += THREADS)
       if (RF_IDX_OK(base + c, (long long)gridDim.x * K8)) xq[base + c] = encode8_exact(x[base + c], s);

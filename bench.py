@@ -537,7 +537,7 @@ def path_gemm(torch, rf, peaks):
             "value": round(tf, 1), "unit": "TFLOP/s", "us_per_call": round(ms * 1e3, 2),
             "us_quant_plus_gemm": round(ms_both * 1e3, 2),
             "incremental_us_per_call": round(ms_inc * 1e3, 2),
-            "roofline": roofline("tensor", tf, fp8_peak, "TFLOP/s", ncu_traffic("fp8_gemm")),
+            "roofline": roofline("tensor", tf, fp8_peak, "TFLOP/s", ncu_traffic("fp8_gemm_2sm")),
             "peak_note": "fp8 peak = 2 x measured bf16 burst (nominal fp8/bf16 ratio)"}
 
 

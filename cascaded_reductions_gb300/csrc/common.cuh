@@ -165,6 +165,8 @@ rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int reno
                               int32_t* idx, float* w, cudaStream_t st);
 rf_status launch_absmax_quant(const void* x, int M, int K, uint8_t* xq, float* sx,
                               cudaStream_t st);
+rf_status launch_fp8_gemm_2sm(const uint8_t* xq, const float* sx, const uint8_t* wq,
+                              const float* sw, int M, int N, int K, void* y, cudaStream_t st);
 rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                           int M, int N, int K, void* y, cudaStream_t st);
 rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,

@@ -237,6 +237,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
 rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
                           int M, int N, int K, void* y, cudaStream_t st) {
+  // CTA pairs (gemm_fp8_2sm.cu) wherever they apply; this kernel otherwise
+  const rf_status pair = launch_fp8_gemm_2sm(xq, sx, wq, sw, M, N, K, y, st);
+  if (pair != RF_ERR_UNSUPPORTED) return pair;
   CUtensorMap ta, tb, tbh;
   if (!tc::make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
                         (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||

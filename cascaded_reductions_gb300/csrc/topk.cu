@@ -5,9 +5,11 @@
 // exp-sum denominator and the k largest entries all come from a single pass
 // over the logits held in registers.
 //
-// Three kernels.  For k <= 2 and E a multiple of 32 up to 128,
+// Four kernels.  For k <= 2 and E a multiple of 32 up to 128,
 // softmax_top2_row_kernel: one thread per token over a row staged in shared
-// memory (below).  For other E <= 128 (with k <= G), softmax_topk_merge_kernel:
+// memory (below).  For E = 256 and k <= 8, softmax_top8_pair_kernel: two
+// threads per token over a staged row (below).  For other E <= 128 (with
+// k <= G), softmax_topk_merge_kernel:
 // each lane keeps its best two logits and the group merges lane heads round by
 // round (below).  Otherwise softmax_topk_kernel:
 //
@@ -51,6 +53,12 @@ constexpr uint32_t FULL = 0xffffffffu;
 __device__ __forceinline__ uint32_t order_key(float x) {
   const uint32_t u = __float_as_uint(x + 0.0f);     // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float key_value(uint32_t k) {
@@ -538,6 +546,188 @@ softmax_top2_row_kernel(const float* __restrict__ logits, int T, int k, int reno
   }
 }
 
+// Two threads per token, for E = 256 and k <= 8.
+//
+// A block of 32 threads stages its 16 rows (1 KiB each) with 16-byte cp.async
+// copies.  Thread h of a token's pair owns experts [128 h, 128 h + 128), the
+// 16-byte chunks [32 h, 32 h + 32) of the row; chunk C of row t lands at
+// position C ^ (2 (t & 3) + C / 32), so the 8-thread phases of the 16-byte
+// loads (four tokens x two halves reading the same chunk offset) hit 8
+// different bank groups.  Per token:
+//   * each thread takes the maxima of its 8 groups of 16 values and sorts
+//     them; the 8 largest of the pair's 16 are max(mine[i], partner[7-i])
+//     (one shuffle each), and thr, the smallest of those, has at least 8
+//     distinct values at or above it: the top 8 all lie at or above thr;
+//   * each thread marks its values >= thr (about six on random logits) and
+//     inserts them, in expert order, into a sorted top-8 of its half
+//     (strict compares: an equal value from a later expert goes after);
+//   * the two halves' lists merge bitonically: max(a[i], b[7-i]) under
+//     (larger value, lower expert), then three compare-exchange stages;
+//     both threads hold the result, and thread h stores entries 4h .. 4h + 3.
+// The top k <= 8 are the first k entries.  Measured against the one-warp
+// selection at [16384 x 256] top-8: 7.05 vs 8.37 us (probe, same inputs).
+// A token with thr = -inf (8 or more experts at -inf) takes the insertion
+// that also fills empty slots with -inf values.
+__device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+template <bool RENORM, int KT>      // KT = k when known at compile time (0: runtime)
+__global__ void __launch_bounds__(32)
+softmax_top8_pair_kernel(const float* __restrict__ logits, int T, int k_rt,
+                         int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+  const int k = KT > 0 ? KT : k_rt;
+  constexpr int E = 256, CH = 64, TOK = 16, KK = 8;
+  constexpr int EMPTY = 0x7fffffff;
+  __shared__ __align__(16) float4 rows[TOK * CH];
+  const int t0 = blockIdx.x * TOK;
+  const int nrows = min(TOK, T - t0);
+  const float4* src = reinterpret_cast<const float4*>(logits) + (size_t)t0 * CH;
+  for (int q = threadIdx.x; q < nrows * CH; q += 32) {
+    const int t = q / CH, c = q % CH;
+    if (RF_SPAN_OK(((size_t)t0 * CH + q) * 4, 4, (long long)T * E)) {
+      const int f = ((t & 3) << 1) | (c >> 5);
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&rows[t * CH + (c ^ f)]);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + q) : "memory");
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  // pairs past the last row work on the last row (the shuffles need every
+  // lane) and store nothing
+  const int tl = min(threadIdx.x >> 1, nrows - 1), h = threadIdx.x & 1;
+  const int f = ((tl & 3) << 1) | h;
+  const float4* row = rows + tl * CH;
+  const float* rowf = reinterpret_cast<const float*>(row);
+  // maxima of the thread's 8 groups of 16 values, sorted descending
+  float sm[8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 v = row[(32 * h + 4 * g + j) ^ f];
+      m = max3f(m, max3f(v.x, v.y, v.z), v.w);
+    }
+    sm[g] = m;
+  }
+  auto cs = [](float& a, float& b) {
+    const float hi = fmaxf(a, b), lo = fminf(a, b);
+    a = hi;
+    b = lo;
+  };
+  cs(sm[0], sm[1]); cs(sm[2], sm[3]); cs(sm[4], sm[5]); cs(sm[6], sm[7]);
+  cs(sm[0], sm[2]); cs(sm[1], sm[3]); cs(sm[4], sm[6]); cs(sm[5], sm[7]);
+  cs(sm[1], sm[2]); cs(sm[5], sm[6]); cs(sm[0], sm[4]); cs(sm[3], sm[7]);
+  cs(sm[1], sm[5]); cs(sm[2], sm[6]);
+  cs(sm[1], sm[4]); cs(sm[3], sm[6]);
+  cs(sm[2], sm[4]); cs(sm[3], sm[5]);
+  cs(sm[3], sm[4]);
+  float thr = INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) thr = fminf(thr, fmaxf(sm[i], __shfl_xor_sync(FULL, sm[7 - i], 1)));
+  const float rmax = fmaxf(sm[0], __shfl_xor_sync(FULL, sm[0], 1));
+  // candidates: values >= thr, one bit per value in expert order
+  uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float4 v = row[(32 * h + c) ^ f];
+    const uint32_t b = (v.x >= thr ? 1u : 0u) | (v.y >= thr ? 2u : 0u) |
+                       (v.z >= thr ? 4u : 0u) | (v.w >= thr ? 8u : 0u);
+    cm[c >> 3] |= b << (4 * (c & 7));
+  }
+  float tv[KK];
+  int ti[KK];
+#pragma unroll
+  for (int i = 0; i < KK; ++i) {
+    tv[i] = -INFINITY;
+    ti[i] = EMPTY;
+  }
+  auto insert = [&](float x, int e, bool any_empty) {
+    bool c[KK];
+#pragma unroll
+    for (int i = 0; i < KK; ++i) c[i] = x > tv[i] || (any_empty && ti[i] == EMPTY);
+#pragma unroll
+    for (int i = KK - 1; i > 0; --i) {
+      tv[i] = c[i] ? (c[i - 1] ? tv[i - 1] : x) : tv[i];
+      ti[i] = c[i] ? (c[i - 1] ? ti[i - 1] : e) : ti[i];
+    }
+    tv[0] = c[0] ? x : tv[0];
+    ti[0] = c[0] ? e : ti[0];
+  };
+  auto insert_all = [&](bool any_empty) {
+#pragma unroll
+    for (int wv = 0; wv < 4; ++wv) {
+      uint32_t m = cm[wv];
+      while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        const int pos = 32 * wv + b;                     // 0..127 within the half
+        insert(rowf[4 * ((32 * h + (pos >> 2)) ^ f) + (pos & 3)], 128 * h + pos, any_empty);
+      }
+    }
+  };
+  // with a finite thr every candidate beats the -inf of an empty slot
+  if (__all_sync(FULL, thr > -INFINITY))
+    insert_all(false);
+  else
+    insert_all(true);
+  // merge the halves: the 8 best of the 16 as a bitonic sequence, then sort
+  float mv[KK];
+  int mi[KK];
+#pragma unroll
+  for (int i = 0; i < KK; ++i) {
+    const float ov = __shfl_xor_sync(FULL, tv[KK - 1 - i], 1);
+    const int oi = __shfl_xor_sync(FULL, ti[KK - 1 - i], 1);
+    const bool mine = ranks_before(tv[i], ti[i], ov, oi);
+    mv[i] = mine ? tv[i] : ov;
+    mi[i] = mine ? ti[i] : oi;
+  }
+  auto cas = [&](int a, int b) {
+    const bool keep = ranks_before(mv[a], mi[a], mv[b], mi[b]);
+    const float va = keep ? mv[a] : mv[b], vb = keep ? mv[b] : mv[a];
+    const int ia = keep ? mi[a] : mi[b], ib = keep ? mi[b] : mi[a];
+    mv[a] = va;
+    mv[b] = vb;
+    mi[a] = ia;
+    mi[b] = ib;
+  };
+  cas(0, 4); cas(1, 5); cas(2, 6); cas(3, 7);
+  cas(0, 2); cas(1, 3); cas(4, 6); cas(5, 7);
+  cas(0, 1); cas(2, 3); cas(4, 5); cas(6, 7);
+  // weights exp(x - m) over the selected (renormalised) or over the row
+  float ex[KK], sel = 0.f;
+#pragma unroll
+  for (int i = 0; i < KK; ++i) {
+    ex[i] = i < k ? __expf(mv[i] - rmax) : 0.f;
+    sel += ex[i];
+  }
+  float denom = sel;
+  if (!RENORM) {
+    float l = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const float4 v = row[(32 * h + c) ^ f];
+      l += __expf(v.x - rmax) + __expf(v.y - rmax) + __expf(v.z - rmax) + __expf(v.w - rmax);
+    }
+    denom = l + __shfl_xor_sync(FULL, l, 1);
+  }
+  const float inv = __fdividef(1.f, denom);
+  if ((int)(threadIdx.x >> 1) < nrows) {
+    const size_t token = (size_t)(t0 + tl);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 4 * h + i;
+      const int id = h ? mi[4 + i] : mi[i];
+      const float wj = (h ? ex[4 + i] : ex[i]) * inv;
+      if (j < k && RF_IDX_OK(token * k + j, (long long)T * k)) {
+        idx_out[token * k + j] = id;
+        w_out[token * k + j] = wj;
+      }
+    }
+  }
+}
+
 template <int E>
 void launch_top2_rows(const float* logits, int T, int k, int renorm, int32_t* idx, float* w,
                       cudaStream_t st) {
@@ -591,6 +781,16 @@ rf_status launch_softmax_topk(const float* logits, int T, int E, int k, int reno
       case 96: launch_top2_rows<96>(logits, T, k, renormalize, idx, w, st); break;
       default: launch_top2_rows<128>(logits, T, k, renormalize, idx, w, st); break;
     }
+    return launch_status();
+  }
+  if (E == 256 && k <= 8) {
+    const unsigned grid = (unsigned)((T + 15) / 16);
+    if (renormalize && k == 8)
+      softmax_top8_pair_kernel<true, 8><<<grid, 32, 0, st>>>(logits, T, k, idx, w);
+    else if (renormalize)
+      softmax_top8_pair_kernel<true, 0><<<grid, 32, 0, st>>>(logits, T, k, idx, w);
+    else
+      softmax_top8_pair_kernel<false, 0><<<grid, 32, 0, st>>>(logits, T, k, idx, w);
     return launch_status();
   }
   // lanes r < k of a group keep round r's winner, so G >= k

@@ -144,3 +144,31 @@ def test_one_thread_per_token_ties_and_order(rf, E):
     for k in (1, 2):
         check(rf, x, k, True, f"ties E={E} k={k}")
         check(rf, x, k, False, f"ties E={E} k={k} no renorm")
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 5, 7, 8])
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 1000])
+def test_two_threads_per_token_shapes(rf, k, T):
+    # E = 256, k <= 8: two threads per token over a staged row; T around the
+    # 16-token block (ragged tails), renormalisation on and off
+    x = si.routing_logits(T, 256, seed=500 + 10 * k + T)
+    check(rf, x, k, True, f"E=256 k={k} T={T}")
+    check(rf, x, k, False, f"E=256 k={k} T={T} no renorm")
+
+
+def test_two_threads_per_token_structure(rf):
+    T, E = 64, 256
+    x = si.routing_logits(T, E, seed=77)
+    x[0, :] = 0.5                             # every value a candidate, all tied
+    x[1, 128:] += 40.0                        # the top 8 all in the second half
+    x[2, :128] += 40.0                        # ... all in the first half
+    x[3, :] = -float("inf")
+    x[3, 5] = 2.0                             # one finite value, the rest -inf ties
+    x[4, :] = -float("inf")
+    x[4, 200:203] = 1.0                       # three finite, ties among the -inf after them
+    x[5, ::2] = -float("inf")                 # half the row at -inf
+    x[6, 127] = x[6, 128] = 30.0              # a tie across the two halves
+    x[7, 0] = x[7, 255] = 30.0
+    for k in (1, 4, 8):
+        check(rf, x, k, True, f"structure k={k}")
+        check(rf, x, k, False, f"structure k={k} no renorm")

@@ -62,7 +62,7 @@ struct Shared {
   uint64_t kv_empty[STAGES];
   uint64_t s_full[2];          // per tile
   uint64_t p_ready[2];         // per tile, 8 softmax warps
-  uint64_t o_done[2];          // per tile
+  uint64_t o_done[2];          // per tile: the last P V done (one phase)
   uint64_t l_ready[2];         // per tile, 8 softmax warps
   float row_l[2][BM];          // [tile][row]: the row's sum, for the epilogue
   float row_m[2][BM];          // [tile][row]: the row's reference max (log2 units)
@@ -121,25 +121,27 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
 }
 
 // S (TMEM) = Q (smem) K^T (smem): eight K-steps of 16 columns; the second 64
-// columns of each tile sit in the second swizzled half
-__device__ __forceinline__ void mma_qk(uint32_t d, uint32_t q_addr, uint32_t k_addr) {
+// columns of each tile sit in the second swizzled half.  The descriptors of
+// the tiles' first K-step are built once by the caller; a K-step's descriptor
+// is that plus its byte offset >> 4 (a compile-time constant), so each MMA
+// costs the issuing thread one 64-bit add instead of a descriptor build.
+__device__ __forceinline__ void mma_qk(uint32_t d, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN, false);
 #pragma unroll
   for (int kk = 0; kk < HD / 16; ++kk) {
-    const uint32_t off = (uint32_t)((kk >> 2) * HALF_BYTES + (kk & 3) * 32);
-    tc::mma_f16_ss(d, tc::sdesc_sw128(q_addr + off, 16, 1024),
-                   tc::sdesc_sw128(k_addr + off, 16, 1024), idesc, kk != 0);
+    const uint64_t off = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+    tc::mma_f16_ss(d, q_desc + off, k_desc + off, idesc, kk != 0);
   }
 }
 
 // O (TMEM) [+]= P (TMEM, 16 keys = 8 columns per step) V (smem, MN-major:
-// 64-column halves 16 KiB apart, 8-key groups 1 KiB apart)
-__device__ __forceinline__ void mma_pv(uint32_t o, uint32_t p, uint32_t v_addr, bool acc) {
+// 64-column halves 16 KiB apart, 8-key groups 1 KiB apart; v_desc is the
+// descriptor of the first 16-key group)
+__device__ __forceinline__ void mma_pv(uint32_t o, uint32_t p, uint64_t v_desc, bool acc) {
   constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, HD, true);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk)
-    tc::mma_f16_ts(o, p + (uint32_t)(kk * 8),
-                   tc::sdesc_sw128(v_addr + (uint32_t)(kk * 2048), HALF_BYTES, 1024), idesc,
+    tc::mma_f16_ts(o, p + (uint32_t)(kk * 8), v_desc + (uint64_t)((kk * 2048) >> 4), idesc,
                    (acc || kk != 0) ? 1u : 0u);
 }
 
@@ -214,7 +216,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------ MMA ----
     if (lane == 0) {
-      const uint32_t q_addr0 = tc::smem_u32(sQ), q_addr1 = tc::smem_u32(sQ + TILE_BYTES);
+      // the first K-step's descriptors of Q_A, Q_B and of each K and V stage
+      const uint64_t q_desc0 = tc::sdesc_sw128(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t q_desc1 = tc::sdesc_sw128(tc::smem_u32(sQ + TILE_BYTES), 16, 1024);
+      static_assert(STAGES == 2, "one descriptor per stage, picked by j & 1");
+      const uint64_t k_desc0 = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+      const uint64_t k_desc1 = tc::sdesc_sw128(tc::smem_u32(sK + TILE_BYTES), 16, 1024);
+      const uint64_t v_desc0 = tc::sdesc_sw128(tc::smem_u32(sV), HALF_BYTES, 1024);
+      const uint64_t v_desc1 = tc::sdesc_sw128(tc::smem_u32(sV + TILE_BYTES), HALF_BYTES, 1024);
       bool ok = tc::mbar_wait(&sh->q_full, 0, abort);
       // S_x(j) needs K_j; the wait is done once per j
       int k_waited = -1;
@@ -225,8 +234,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             return false;
         }
         tc::fence_after_sync();
-        mma_qk(tmem + s_col(x), x ? q_addr1 : q_addr0,
-               tc::smem_u32(sK + (j % STAGES) * TILE_BYTES));
+        mma_qk(tmem + s_col(x), x ? q_desc1 : q_desc0, (j & 1) ? k_desc1 : k_desc0);
         tc::mma_commit(&sh->s_full[x]);
         return true;
       };
@@ -239,9 +247,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
             return false;
         }
         tc::fence_after_sync();
-        mma_pv(tmem + o_col(x), tmem + s_col(x), tc::smem_u32(sV + (j % STAGES) * TILE_BYTES),
-               j > 0);
-        tc::mma_commit(&sh->o_done[x]);
+        mma_pv(tmem + o_col(x), tmem + s_col(x), (j & 1) ? v_desc1 : v_desc0, j > 0);
+        // a tile's softmax learns that P V(j) is done from S(j + 1)'s commit
+        // (every commit covers all earlier MMAs of this thread); only the last
+        // P V needs a commit of its own, for the epilogue
+        if (j == (x ? nblk1 : nblk0) - 1) tc::mma_commit(&sh->o_done[x]);
         return true;
       };
       if (ok) ok = issue_s(0, 0);
@@ -360,13 +370,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
         l[0] += lo_f32(sum2[0]) + hi_f32(sum2[0]);
         l[1] += lo_f32(sum2[1]) + hi_f32(sum2[1]);
       }
-      // O must hold every earlier P V before it is rescaled
+      // O holds every earlier P V before it is rescaled: S(j) was issued after
+      // P V(j - 1), and its completion (waited above) covers it
       if (j > 0) {
-        if (!tc::mbar_wait(&sh->o_done[x], (uint32_t)(j - 1) & 1u, abort)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
         if (__any_sync(0xffffffffu, move_any)) {
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
@@ -410,7 +416,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
       // writes columns 64 sub .. 64 sub + 63 of rows 32 quarter .. + 31.
       // out = O / l, lse = (m_ref + log2 l) * ln 2
       if (ok && tc::mbar_wait(&sh->l_ready[x], 0, abort) &&
-          tc::mbar_wait(&sh->o_done[x], (uint32_t)(n - 1) & 1u, abort)) {
+          tc::mbar_wait(&sh->o_done[x], 0, abort)) {
         tc::fence_after_sync();
         const int r = quarter * 32 + lane;
         const int col0 = sub * 64;

@@ -16,9 +16,12 @@
 //
 // Persistent, one CTA per SM, warp-specialised (both CTAs of a pair run the
 // same roles):
-//   warp 0      TMA producer: this CTA's 128 x 128-byte Xq rows and 128 x
-//               128-byte Wq rows into a 6-stage ring; the copies of both CTAs
-//               complete on CTA 0's stage barrier;
+//   warp 0      TMA producer: this CTA's 128 x 256-byte Xq rows and 128 x
+//               256-byte Wq rows (each as two 128-byte-swizzled sub-tiles)
+//               into a 3-stage ring; the copies of both CTAs complete on CTA
+//               0's stage barrier.  256 bytes of K per stage: the issuing
+//               thread's wait, fence and commit per stage cost the tensor pipe
+//               idle time, so a stage carries eight MMAs rather than four;
 //   warp 1      TMEM allocation for the pair (512 columns: two 256-column
 //               accumulators); in CTA 0 one thread issues the MMAs, commits
 //               each stage to both CTAs' producers and each finished
@@ -41,11 +44,14 @@ namespace {
 
 constexpr int BM = 128;                       // rows per CTA (256 per pair)
 constexpr int BN = 256;                       // columns per pair tile
-constexpr int BK = 128;                       // bytes = e4m3 elements per stage
+constexpr int BK = 256;                       // bytes = e4m3 elements per stage
+constexpr int SUB = 128;                      // K bytes per 128-byte-swizzled sub-tile
 constexpr int UMMA_K = 32;
-constexpr int STAGES = 6;
-constexpr int A_BYTES = BM * BK;              // 16 KiB: this CTA's Xq rows
-constexpr int B_BYTES = (BN / 2) * BK;        // 16 KiB: this CTA's half of the Wq tile
+constexpr int STAGES = 3;
+constexpr int A_SUB = BM * SUB;               // 16 KiB: this CTA's Xq rows, one sub-tile
+constexpr int B_SUB = (BN / 2) * SUB;         // 16 KiB: this CTA's half of the Wq tile, one sub-tile
+constexpr int A_BYTES = 2 * A_SUB;            // 32 KiB
+constexpr int B_BYTES = 2 * B_SUB;            // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
@@ -176,6 +182,7 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         item(i, tm2, col0, width);
         const bool half = width != BN;
         const uint32_t bytes = 2u * (uint32_t)(A_BYTES + (half ? B_BYTES / 2 : B_BYTES));
+        const int bw = width / 2;                   // rows of B this CTA loads
         for (int kb = 0; kb < num_k; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -183,9 +190,13 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t full0 = tc::mapa(tc::smem_u32(&sh->full[s]), 0);
           if (rank == 0) tc::mbar_arrive_expect_tx(&sh->full[s], bytes);
           uint8_t* a = smem + (size_t)s * STAGE_BYTES;
-          tma_load_2d_pair(a, &tmA, full0, kb * BK, tm2 * 2 * BM + rank * BM);
-          tma_load_2d_pair(a + A_BYTES, half ? &tmBh : &tmB, full0, kb * BK,
-                           col0 + rank * (width / 2));
+          uint8_t* b = a + A_BYTES;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d_pair(a + h * A_SUB, &tmA, full0, kb * BK + h * SUB, tm2 * 2 * BM + rank * BM);
+            tma_load_2d_pair(b + h * (half ? B_SUB / 2 : B_SUB), half ? &tmBh : &tmB, full0,
+                             kb * BK + h * SUB, col0 + rank * bw);
+          }
         }
       }
     }
@@ -214,10 +225,15 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t a = tc::smem_u32(smem + (size_t)s * STAGE_BYTES);
           const uint64_t adesc = tc::sdesc_sw128(a, 16, 1024);
           const uint64_t bdesc = tc::sdesc_sw128(a + A_BYTES, 16, 1024);
+          // the B sub-tiles of a half-width item are half as tall
+          const uint64_t b_sub = (uint64_t)((i < full_items ? B_SUB : B_SUB / 2) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k)
-            mma_pair(d, adesc + (uint64_t)(k * UMMA_K / 16), bdesc + (uint64_t)(k * UMMA_K / 16),
-                     idesc, (kb | k) != 0);
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const int h = k / (SUB / UMMA_K), kk = k % (SUB / UMMA_K);
+            mma_pair(d, adesc + (uint64_t)((h * A_SUB + kk * UMMA_K) >> 4),
+                     bdesc + (uint64_t)h * b_sub + (uint64_t)((kk * UMMA_K) >> 4), idesc,
+                     (kb | k) != 0);
+          }
           commit_pair_both(&sh->empty[s]);
         }
         if (!ok) break;
@@ -344,11 +360,11 @@ rf_status launch_fp8_gemm_2sm(const uint8_t* xq, const float* sx, const uint8_t*
   if (pairs <= 0) return RF_ERR_UNSUPPORTED;
   CUtensorMap ta, tb, tbh;
   if (!tc::make_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, (uint64_t)K, (uint64_t)M,
-                        (uint64_t)K, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                        (uint64_t)K, SUB, BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
-                        (uint64_t)K, BK, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                        (uint64_t)K, SUB, BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, (uint64_t)K, (uint64_t)N,
-                        (uint64_t)K, BK, BN / 4, CU_TENSOR_MAP_SWIZZLE_128B))
+                        (uint64_t)K, SUB, BN / 4, CU_TENSOR_MAP_SWIZZLE_128B))
     return RF_ERR_CUDA;
   const int tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
   const int clusters = pairs < tiles ? pairs : tiles;

@@ -44,14 +44,15 @@ namespace {
 
 constexpr int BM = 128;                       // rows per CTA (256 per pair)
 constexpr int BN = 256;                       // columns per pair tile
-constexpr int BK = 256;                       // bytes = e4m3 elements per stage
-constexpr int SUB = 128;                      // K bytes per 128-byte-swizzled sub-tile
+constexpr int NSUB = 2;                       // 128-byte-swizzled sub-tiles per operand and stage
+constexpr int SUB = 128;                      // K bytes per sub-tile
+constexpr int BK = NSUB * SUB;                // bytes = e4m3 elements per stage
 constexpr int UMMA_K = 32;
 constexpr int STAGES = 3;
 constexpr int A_SUB = BM * SUB;               // 16 KiB: this CTA's Xq rows, one sub-tile
 constexpr int B_SUB = (BN / 2) * SUB;         // 16 KiB: this CTA's half of the Wq tile, one sub-tile
-constexpr int A_BYTES = 2 * A_SUB;            // 32 KiB
-constexpr int B_BYTES = 2 * B_SUB;            // 32 KiB
+constexpr int A_BYTES = NSUB * A_SUB;
+constexpr int B_BYTES = NSUB * B_SUB;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int THREADS = 192;
@@ -192,7 +193,7 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           uint8_t* a = smem + (size_t)s * STAGE_BYTES;
           uint8_t* b = a + A_BYTES;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < NSUB; ++h) {
             tma_load_2d_pair(a + h * A_SUB, &tmA, full0, kb * BK + h * SUB, tm2 * 2 * BM + rank * BM);
             tma_load_2d_pair(b + h * (half ? B_SUB / 2 : B_SUB), half ? &tmBh : &tmB, full0,
                              kb * BK + h * SUB, col0 + rank * bw);

@@ -69,58 +69,6 @@ struct Shared {
 constexpr size_t SMEM_BYTES = (size_t)STAGES * STAGE_BYTES + sizeof(Shared) + 1024;
 static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB of shared memory a CTA may use");
 
-// ------------------------------------------------ pair-mode instructions ----
-// TMA load into this CTA's shared memory whose completion is counted on a
-// barrier of either CTA of the pair (`bar`: a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar,
-                                                 int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(tc::smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-      : "memory");
-}
-
-// D (TMEM of both CTAs) [+]= A (shared memory of both CTAs) * B (both), e4m3
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// arrive on the barrier at this offset in both CTAs once the pair MMAs issued
-// so far have completed
-__device__ __forceinline__ void commit_pair_both(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(tc::smem_u32(bar)),
-      "h"((uint16_t)3)
-      : "memory");
-}
-
-// plain arrive on a barrier of either CTA (shared::cluster address)
-__device__ __forceinline__ void arrive_cluster(uint32_t bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
-               : "memory");
-}
-
-// executed by one warp of each CTA of the pair
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   tc::smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBh, const float* __restrict__ sx,
@@ -165,7 +113,7 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc::prefetch_tmap(&tmB);
     tc::prefetch_tmap(&tmBh);
   }
-  if (warp == 1) tmem_alloc_pair(&sh->tmem_base, TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc_pair(&sh->tmem_base, TMEM_COLS);
   tc::fence_before_sync();
   // both CTAs' barriers are initialised before any copy, commit or arrival
   // reaches them
@@ -194,8 +142,8 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           uint8_t* b = a + A_BYTES;
 #pragma unroll
           for (int h = 0; h < NSUB; ++h) {
-            tma_load_2d_pair(a + h * A_SUB, &tmA, full0, kb * BK + h * SUB, tm2 * 2 * BM + rank * BM);
-            tma_load_2d_pair(b + h * (half ? B_SUB / 2 : B_SUB), half ? &tmBh : &tmB, full0,
+            tc::tma_load_2d_pair(a + h * A_SUB, &tmA, full0, kb * BK + h * SUB, tm2 * 2 * BM + rank * BM);
+            tc::tma_load_2d_pair(b + h * (half ? B_SUB / 2 : B_SUB), half ? &tmBh : &tmB, full0,
                              kb * BK + h * SUB, col0 + rank * bw);
           }
         }
@@ -231,14 +179,14 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const int h = k / (SUB / UMMA_K), kk = k % (SUB / UMMA_K);
-            mma_pair(d, adesc + (uint64_t)((h * A_SUB + kk * UMMA_K) >> 4),
+            tc::mma_pair_f8f6f4(d, adesc + (uint64_t)((h * A_SUB + kk * UMMA_K) >> 4),
                      bdesc + (uint64_t)h * b_sub + (uint64_t)((kk * UMMA_K) >> 4), idesc,
                      (kb | k) != 0);
           }
-          commit_pair_both(&sh->empty[s]);
+          tc::commit_pair_both(&sh->empty[s]);
         }
         if (!ok) break;
-        commit_pair_both(&sh->acc_full[buf]);
+        tc::commit_pair_both(&sh->acc_full[buf]);
       }
     }
   } else {
@@ -295,7 +243,7 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) arrive_cluster(buf ? acc_empty0_1 : acc_empty0_0);
+      if (lane == 0) tc::arrive_cluster(buf ? acc_empty0_1 : acc_empty0_0);
     }
   }
 
@@ -310,7 +258,7 @@ fp8_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
     }
     tc::fence_after_sync();
-    tmem_dealloc_pair(tmem, TMEM_COLS);
+    tc::tmem_dealloc_pair(tmem, TMEM_COLS);
   }
 }
 

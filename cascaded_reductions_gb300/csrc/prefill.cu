@@ -465,6 +465,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ 
 rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
                          int causal, float scale, void* out, float* lse, cudaStream_t st) {
   (void)D;
+  const rf_status pair = launch_prefill_2sm(q, k, v, B, H, N, causal, scale, out, lse, st);
+  if (pair != RF_ERR_UNSUPPORTED) return pair;
   const uint64_t rows = (uint64_t)B * H * N;
   CUtensorMap tq, tk, tv;
   const uint64_t stride = HD * 2;

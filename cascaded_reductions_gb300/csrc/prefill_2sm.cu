@@ -47,6 +47,12 @@
 // written and that O was read with relaxed arrivals: each follows the
 // tcgen05.wait that completes those TMEM accesses, so it needs no release
 // (a release at cluster scope costs the arriving warp about 1000 cycles).
+// For the same reason the MMA thread waits at CTA scope: what it orders
+// after a wait are MMAs, whose operands were completed by the TMA
+// transaction count or by the softmax warps' tcgen05.wait (an acquire at
+// cluster scope idles the tensor pipe about 160 cycles per wait).
+// An item's epilogue is deferred into the first block of the next item (see
+// the softmax role).
 // Every barrier wait is bounded (see tc_common.cuh); the two CTAs meet at a
 // cluster barrier before either exits.
 
@@ -138,35 +144,6 @@ __device__ __forceinline__ void arrive_cluster_relaxed(uint32_t bar) {
                : "memory");
 }
 
-// Wait on a barrier of this CTA that the other CTA of the pair arrives on:
-// the acquire is at cluster scope.  Bounded like tc::mbar_wait.
-__device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(tc::smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = tc::globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (try_wait_cluster(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort) return false;
-      if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
-        *abort = 1;
-        atomicExch(&tc::g_timeout_status, (int)RF_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 // A work item: 256 query rows (two 128-row tiles) of one head.  Items are
 // numbered head-major, the heaviest pair of tiles of each head first.
 struct Item {
@@ -174,6 +151,7 @@ struct Item {
   int pair;     // tiles 2 pair and 2 pair + 1 of the head
   int n;        // key blocks (the same for both CTAs)
 };
+
 // Cluster c takes the item c of every even round of nclusters items and
 // item nclusters - 1 - c of every odd round: with items weighted p + 1 under
 // the causal mask, the snake evens out the clusters' totals (plain
@@ -296,7 +274,7 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // item's last S also releases its Q buffer.
       auto issue_s = [&](uint32_t g, int qb, bool last_of_item) -> bool {
         const int s = (int)(g & 1u);
-        if (!wait_cluster(&sh->k_full[s], (g >> 1) & 1u, abort)) return false;
+        if (!tc::mbar_wait(&sh->k_full[s], (g >> 1) & 1u, abort)) return false;
         tc::fence_after_sync();
         const uint64_t kd = s ? k_desc1 : k_desc0;
         const uint64_t qd = qb ? q_desc1 : q_desc0;
@@ -313,7 +291,7 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // O [+]= P V(g): sixteen K-steps of 16 keys (8 TMEM columns of P, 2 KiB of V)
       auto issue_pv = [&](uint32_t g, bool accumulate) -> bool {
         const int s = (int)(g & 1u);
-        if (!wait_cluster(&sh->v_full[s], (g >> 1) & 1u, abort)) return false;
+        if (!tc::mbar_wait(&sh->v_full[s], (g >> 1) & 1u, abort)) return false;
         tc::fence_after_sync();
         const uint64_t vd = s ? v_desc1 : v_desc0;
 #pragma unroll
@@ -330,7 +308,7 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       bool ok = item_index(0, cluster, nclusters) < num_items;
       if (ok) {
         const Item first = item_of(item_index(0, cluster, nclusters), N, causal);
-        ok = wait_cluster(&sh->q_full[0], 0, abort) && issue_s(0, 0, first.n == 1);
+        ok = tc::mbar_wait(&sh->q_full[0], 0, abort) && issue_s(0, 0, first.n == 1);
       }
       uint32_t g = 0;
       for (int t = 0; ok; ++t) {
@@ -340,25 +318,24 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int i_next = item_index(t + 1, cluster, nclusters);
         const bool has_next = i_next < num_items;
         for (int j = 0; ok && j < it.n; ++j, ++g) {
-          if (j + 1 < it.n) {
+          if (j + 1 < it.n || has_next) {
             // S(g + 1) overwrites S(g): both CTAs' softmax warps have read it
-            if (!(ok = wait_cluster(&sh->s_free, g & 1u, abort))) break;
-            if (!(ok = issue_s(g + 1, t & 1, j + 2 == it.n))) break;
+            if (!(ok = tc::mbar_wait(&sh->s_free, g & 1u, abort))) break;
+            if (j + 1 < it.n) {
+              ok = issue_s(g + 1, t & 1, j + 2 == it.n);
+            } else {
+              const int n_next = item_of(i_next, N, causal).n;
+              const int qb = (t + 1) & 1;
+              ok = tc::mbar_wait(&sh->q_full[qb], ((uint32_t)(t + 1) >> 1) & 1u, abort) &&
+                   issue_s(g + 1, qb, n_next == 1);
+            }
+            if (!ok) break;
           }
-          if (!(ok = wait_cluster(&sh->p_ready, g & 1u, abort))) break;
-          // the item's first P V overwrites O: the last item's epilogue has read it
-          if (j == 0 && t > 0 && !(ok = wait_cluster(&sh->o_free, (uint32_t)(t - 1) & 1u, abort)))
+          if (!(ok = tc::mbar_wait(&sh->p_ready, g & 1u, abort))) break;
+          // the item's first P V overwrites O: the last item's O has been read
+          if (j == 0 && t > 0 && !(ok = tc::mbar_wait(&sh->o_free, (uint32_t)(t - 1) & 1u, abort)))
             break;
-          if (!(ok = issue_pv(g, j > 0))) break;
-          if (j + 1 == it.n && has_next) {
-            // the next item's first S goes after this item's last P V, which
-            // the epilogue waits for; it is computed while the epilogue runs
-            const int n_next = item_of(i_next, N, causal).n;
-            const int qb = (t + 1) & 1;
-            ok = wait_cluster(&sh->s_free, g & 1u, abort) &&
-                 wait_cluster(&sh->q_full[qb], ((uint32_t)(t + 1) >> 1) & 1u, abort) &&
-                 issue_s(g + 1, qb, n_next == 1);
-          }
+          ok = issue_pv(g, j > 0);
         }
       }
     }
@@ -375,6 +352,60 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const bool out32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
     uint32_t g = 0, x = 0;                          // blocks and red_bar exchanges so far
     bool ok = true;
+    const long long heads = (long long)num_items / ((((N + BM - 1) / BM) + 1) / 2);
+    (void)heads;                                    // read by the checked build only
+    // The epilogue of an item is deferred into the first block of the next:
+    // O is read there (once the item's last P V is done, which the new
+    // block's P has to wait for anyway), released for the next item's first
+    // P V, and written out after the new P is handed over.
+    bool pend = false;                              // an item's output is still to be written
+    float pend_m = 0.f, pend_l = 0.f;
+    int pend_row = 0;                               // global query row
+    bool pend_in = false;                           // the row belongs to a query
+    auto take_o = [&](uint32_t g_last, uint32_t (&v)[32]) -> bool {
+      if (!tc::mbar_wait(&sh->pv_done, g_last & 1u, abort)) return false;
+      tc::fence_after_sync();
+      tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kq * 32), v);
+      tc::tmem_ld_wait();
+      // O is in registers: the next item's first P V may overwrite it
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_cluster_relaxed(o_free0);
+      return true;
+    };
+    // the row's sum over its four warps; out = O / l and lse = (m_ref +
+    // log2 l) ln 2.  Warp (quarter, kq) writes columns 32 kq .. + 31 of rows
+    // 32 quarter .. + 31.
+    auto finish = [&](const uint32_t (&v)[32]) -> bool {
+      sh->part_l[kq][r] = pend_l;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->red_bar[quarter]);
+      if (!tc::mbar_wait(&sh->red_bar[quarter], x & 1u, abort)) return false;
+      ++x;
+      const float lt = (sh->part_l[0][r] + sh->part_l[1][r]) + (sh->part_l[2][r] + sh->part_l[3][r]);
+      const float inv = 1.f / lt;
+      uint32_t pkd[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        pkd[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
+      // (checked build) 32 outputs inside out[B*H][N][HD]
+      if (pend_in && RF_SPAN_OK((size_t)pend_row * HD + kq * 32, 32, heads * N * HD)) {
+        __nv_bfloat16* dst = out + (size_t)pend_row * HD + kq * 32;
+        if (out32) {
+          // 32-byte stores: each fills one sector of the row
+          st_global_v8(dst, pkd);
+          st_global_v8(dst + 16, pkd + 8);
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            d4[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+        }
+      }
+      if (lse != nullptr && kq == 0 && pend_in && RF_IDX_OK(pend_row, heads * N))
+        lse[pend_row] = (pend_m + log2f(lt)) * kLn2;
+      return true;
+    };
     for (int t = 0; ok; ++t) {
       const int i = item_index(t, cluster, nclusters);
       if (i >= num_items) break;
@@ -471,56 +502,44 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             tc::tmem_st_32x32b_x32(oc, v);
           }
         }
+        const bool have_o = j == 0 && pend;
+        if (have_o) {
+          // P and O are the previous item's until its last P V is done
+          if (!(ok = tc::mbar_wait(&sh->pv_done, (g - 1) & 1u, abort))) break;
+          tc::fence_after_sync();
+        }
         tc::tmem_st_32x32b_x32(lanes + P_COL + (uint32_t)(kq * 32), w);
         tc::tmem_st_wait();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) arrive_cluster_relaxed(p_ready0);
-      }
-      if (!ok) break;
-      // epilogue: the row's sum over its four warps; out = O / l and
-      // lse = (m_ref + log2 l) ln 2.  Warp (quarter, kq) writes columns
-      // 32 kq .. + 31 of rows 32 quarter .. + 31.
-      sh->part_l[kq][r] = l;
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->red_bar[quarter]);
-      if (!(ok = tc::mbar_wait(&sh->red_bar[quarter], x & 1u, abort))) break;
-      ++x;
-      if (!(ok = tc::mbar_wait(&sh->pv_done, (g - 1) & 1u, abort))) break;
-      tc::fence_after_sync();
-      uint32_t v[32];
-      tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kq * 32), v);
-      tc::tmem_ld_wait();
-      // O is in registers: the next item's first P V may overwrite it
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) arrive_cluster_relaxed(o_free0);
-      const float lt = (sh->part_l[0][r] + sh->part_l[1][r]) + (sh->part_l[2][r] + sh->part_l[3][r]);
-      const float inv = 1.f / lt;
-      const int grow = it.key0 + m_tile * BM + r;   // global query row
-      const bool row_in = m_tile * BM + r < N;      // rows past N belong to no query
-      uint32_t pkd[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pkd[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
-      const long long heads = (long long)num_items / ((((N + BM - 1) / BM) + 1) / 2);
-      (void)heads;                                  // read by the checked build only
-      // (checked build) 32 outputs inside out[B*H][N][HD]
-      if (row_in && RF_SPAN_OK((size_t)grow * HD + kq * 32, 32, heads * N * HD)) {
-        __nv_bfloat16* dst = out + (size_t)grow * HD + kq * 32;
-        if (out32) {
-          // 32-byte stores: each fills one sector of the row
-          st_global_v8(dst, pkd);
-          st_global_v8(dst + 16, pkd + 8);
+        if (have_o) {
+          uint32_t ov[32];                          // the previous item's O
+          tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kq * 32), ov);
+          tc::tmem_ld_wait();
+          // O is in registers and P is written: the first P V of this item
+          // may go
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            arrive_cluster_relaxed(o_free0);
+            arrive_cluster_relaxed(p_ready0);
+          }
+          if (!(ok = finish(ov))) break;
+          pend = false;
         } else {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            d4[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) arrive_cluster_relaxed(p_ready0);
         }
       }
-      if (lse != nullptr && kq == 0 && row_in && RF_IDX_OK(grow, heads * N))
-        lse[grow] = (m_ref + log2f(lt)) * kLn2;
+      if (!ok) break;
+      pend = true;
+      pend_m = m_ref;
+      pend_l = l;
+      pend_row = it.key0 + m_tile * BM + r;
+      pend_in = m_tile * BM + r < N;              // rows past N belong to no query
+    }
+    if (ok && pend) {
+      uint32_t ov[32];
+      if (take_o(g - 1, ov)) finish(ov);
     }
   }
 

@@ -24,7 +24,8 @@
 // One CTA per 128 x 512 block of Y; 512 TMEM columns hold the accumulator as
 // two halves of 256 columns, so that one half is rescaled while the tensor
 // core works on the other.
-//   warp 0       TMA: e4m3 Wq half tiles (256 rows, 4-stage ring);
+//   warp 0       TMA: e4m3 Wq tiles (two 256-row halves on one barrier,
+//                2-tile ring);
 //   warp 1       TMEM allocation and the MMAs (128x256x32, one half of the
 //                accumulator at a time), committing A stages to every CTA of
 //                the cluster;
@@ -74,7 +75,7 @@ struct Cfg {
 
 struct Shared {
   float2 fac[A_STAGES][BM];       // per A stage and row: {s / s' (1 if unchanged), s'}
-  uint64_t w_full[W_STAGES], w_empty[W_STAGES];
+  uint64_t w_full[W_STAGES / 2], w_empty[W_STAGES / 2];   // per tile slot (two half tiles)
   uint64_t a_full[A_STAGES];      // own band written + the other CTAs' bands stored in
   uint64_t a_empty[A_STAGES];     // one MMA commit from each CTA of the cluster
   uint64_t mma_done[2];           // per accumulator half
@@ -143,7 +144,7 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
       tc::mbar_init(&sh->a_full[s], CONV_WARPS);
       tc::mbar_init(&sh->a_empty[s], C);
     }
-    for (int q = 0; q < W_STAGES; ++q) {
+    for (int q = 0; q < W_STAGES / 2; ++q) {
       tc::mbar_init(&sh->w_full[q], 1);
       tc::mbar_init(&sh->w_empty[q], 1);
     }
@@ -166,11 +167,13 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
     // ------------------------------------------------------ TMA ----
     if (lane == 0) {
       tc::prefetch_tmap(&tmW);
-      for (int i = 0; i < 2 * T; ++i) {        // half tile i: tile i / 2, rows (i % 2) * 256
-        const int q = i % W_STAGES;
-        if (!tc::mbar_wait(&sh->w_empty[q], ((uint32_t)(i / W_STAGES) & 1u) ^ 1u, abort)) break;
-        tc::mbar_arrive_expect_tx(&sh->w_full[q], W_BYTES);
-        tc::tma_load_2d(sW + q * W_BYTES, &tmW, &sh->w_full[q], (i >> 1) * BK, n0 + (i & 1) * 256);
+      for (int t = 0; t < T; ++t) {            // both 256-row halves of tile t on one barrier
+        const int q = t % (W_STAGES / 2);
+        if (!tc::mbar_wait(&sh->w_empty[q], ((uint32_t)(t / (W_STAGES / 2)) & 1u) ^ 1u, abort))
+          break;
+        tc::mbar_arrive_expect_tx(&sh->w_full[q], 2 * W_BYTES);
+        tc::tma_load_2d(sW + (2 * q) * W_BYTES, &tmW, &sh->w_full[q], t * BK, n0);
+        tc::tma_load_2d(sW + (2 * q + 1) * W_BYTES, &tmW, &sh->w_full[q], t * BK, n0 + 256);
       }
     }
   } else if (warp == 1) {
@@ -185,22 +188,20 @@ fp8_incremental_cluster_kernel(const __nv_bfloat16* __restrict__ x,
         if (!(ok = tc::mbar_wait(&sh->a_full[s], ph, abort))) break;
         // the other CTAs' codes were stored into this stage by st.async
         tc::fence_proxy_async_cta();
-        const uint32_t a_addr = tc::smem_u32(sA + s * A_BYTES);
+        const uint64_t a_desc = tc::sdesc_sw128(tc::smem_u32(sA + s * A_BYTES), 16, 1024);
+        const int q = t % (W_STAGES / 2);
+        if (!(ok = tc::mbar_wait(&sh->w_full[q], (uint32_t)(t / (W_STAGES / 2)) & 1u, abort))) break;
         for (int h = 0; h < 2; ++h) {
-          const int i = 2 * t + h, q = i % W_STAGES;
-          if (!(ok = tc::mbar_wait(&sh->w_full[q], (uint32_t)(i / W_STAGES) & 1u, abort))) break;
           // the rescale warps have brought this half up to the scale of tile t
           if (!(ok = tc::mbar_wait(&sh->resc_done[h], (uint32_t)t & 1u, abort))) break;
           tc::fence_after_sync();
-          const uint32_t w_addr = tc::smem_u32(sW + q * W_BYTES);
+          const uint64_t w_desc = tc::sdesc_sw128(tc::smem_u32(sW + (2 * q + h) * W_BYTES), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < BK / 32; ++kk)
-            tc::mma_f8f6f4_ss(tmem + (uint32_t)(h * 256),
-                              tc::sdesc_sw128(a_addr + (uint32_t)(kk * 32), 16, 1024),
-                              tc::sdesc_sw128(w_addr + (uint32_t)(kk * 32), 16, 1024), idesc,
-                              (t | kk) != 0);
+            tc::mma_f8f6f4_ss(tmem + (uint32_t)(h * 256), a_desc + (uint64_t)((kk * 32) >> 4),
+                              w_desc + (uint64_t)((kk * 32) >> 4), idesc, (t | kk) != 0);
           tc::mma_commit(&sh->mma_done[h]);
-          tc::mma_commit(&sh->w_empty[q]);
+          if (h == 1) tc::mma_commit(&sh->w_empty[q]);
         }
         if (!ok) break;
         // this CTA is done with A stage s: tell every converter of the cluster

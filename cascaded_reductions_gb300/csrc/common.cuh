@@ -171,9 +171,6 @@ rf_status launch_fp8_gemm(const uint8_t* xq, const float* sx, const uint8_t* wq,
                           int M, int N, int K, void* y, cudaStream_t st);
 rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
                          int causal, float scale, void* out, float* lse, cudaStream_t st);
-// the same on CTA pairs; RF_ERR_UNSUPPORTED when clusters of two do not fit
-rf_status launch_prefill_2sm(const void* q, const void* k, const void* v, int B, int H, int N,
-                             int causal, float scale, void* out, float* lse, cudaStream_t st);
 rf_status launch_row_softmax(const float* x, int R, int n, float* y, int level, float* work,
                              cudaStream_t st);
 rf_status launch_row_variance(const float* x, int R, int n, float* mean, float* var, int level,

@@ -596,10 +596,11 @@ int resident_pairs() {
 
 }  // namespace
 
-// RF_ERR_UNSUPPORTED when clusters of two do not fit (the one-SM kernel in
-// prefill.cu takes the call).
-rf_status launch_prefill_2sm(const void* q, const void* k, const void* v, int B, int H, int N,
-                             int causal, float scale, void* out, float* lse, cudaStream_t st) {
+// RF_ERR_UNSUPPORTED when a cluster of two of these CTAs cannot be resident
+// on the device (or the item count overflows an int).
+rf_status launch_prefill(const void* q, const void* k, const void* v, int B, int H, int N, int D,
+                         int causal, float scale, void* out, float* lse, cudaStream_t st) {
+  (void)D;                                      // 128, checked by the caller
   const int pairs = resident_pairs();
   if (pairs <= 0) return RF_ERR_UNSUPPORTED;
   const uint64_t rows = (uint64_t)B * H * N;

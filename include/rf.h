@@ -166,8 +166,10 @@ rf_status rf_mla_decode_split(const void* q, const void* c, int B, int H, int L,
  * rf_attn_prefill -- causal prefill attention, GEMM -> online softmax -> GEMM
  * (transcript cue 9: attention stacks a GEMM, then softmax, then another GEMM;
  * cue 31: the incremental form sits at the block level of the reduction tree).
- * Each 128-row query tile streams its K/V tiles once: S = Q K^T * scale on
- * the tensor cores, running (m, l) per row, O = c*O + P V, out = O / l.
+ * Each 128-row query tile streams its K/V blocks once: S = Q K^T * scale on
+ * the tensor cores, running (m, l) per row, O = c*O + P V, out = O / l.  The
+ * kernel runs on clusters of two CTAs (two adjacent query tiles of a head
+ * share every K/V block).
  *
  *   q, k, v   [B, H, N, D]  bf16        D = 128
  *   causal    1: query i sees keys 0..i (top-left aligned); 0: all keys
@@ -177,7 +179,9 @@ rf_status rf_mla_decode_split(const void* q, const void* c, int B, int H, int L,
  * Any N >= 1: the last query and key tiles of a head are partial (keys past
  * N are left out, rows past N are not stored).
  * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
- * RF_ERR_UNSUPPORTED unless D = 128 and B*H*N < 2^31.
+ * RF_ERR_UNSUPPORTED unless D = 128 and B*H*N < 2^31, or when a cluster of
+ * two CTAs with about 200 KiB of shared memory each cannot be launched on
+ * the device.
  */
 rf_status rf_attn_prefill(const void* q, const void* k, const void* v,
                           int B, int H, int N, int D, int causal, float scale,

@@ -5,7 +5,8 @@ through the C ABI.  out is bf16 (|g - r| <= 2e-2 + 1e-2 |r|); lse is fp32
 Cases: one tile (N = 128) causal and not; several key tiles so the K/V ring
 and the two S buffers wrap; ragged lengths (N = 1 … 1000, not multiples of
 128) causal and not; several batches and heads; peaked scores (large
-scale) that move the running max often; the full workload B=4, H=32,
+scale) that move the running max often; enough heads that every
+persistent cluster takes several work items; the full workload B=4, H=32,
 N=8192 with sampled rows compared one by one, and its closed form (causal
 row 0 equals V row 0 exactly).
 """
@@ -66,6 +67,15 @@ def test_ragged_lengths(rf, N, causal):
 
 def test_batches_and_heads(rf):
     check_all(rf, 2, 3, 512, True, seed=7)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_several_items_per_cluster(rf, causal):
+    # 2 x 64 heads of 5 tiles (3 pairs, the last one half past N): 384 work
+    # items, several per persistent cluster, so Q buffers alternate, the
+    # epilogue of one item runs inside the next item's first block, and the
+    # items of a cluster differ in key-block count (causal)
+    check_all(rf, 2, 64, 600, causal, seed=11)
 
 
 def test_peaked_scores(rf):

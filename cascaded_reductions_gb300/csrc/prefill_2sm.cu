@@ -31,14 +31,18 @@
 // Shared memory per CTA: Q tiles (two buffers), K halves and V halves in
 // 2-stage rings, 32 KiB each, all 128-byte swizzled.
 // Roles, both CTAs:
-//   warp 16     TMA: this CTA's Q tile, then its halves of K_j and V_j; the
+//   warp 8      TMA: this CTA's Q tile, then its halves of K_j and V_j; the
 //               copies of both CTAs complete on CTA 0's barriers;
-//   warp 17     TMEM allocation; in CTA 0 one thread issues every MMA and
+//   warp 9      TMEM allocation; in CTA 0 one thread issues every MMA and
 //               commits to both CTAs' barriers;
-//   warps 0-15  softmax of this CTA's 128 rows: warp w reads TMEM lanes
-//               32 (w % 4) .. + 31 (thread = row) and keys 64 (w / 4) .. + 63
-//               of the block; the four warps of a row exchange their partial
-//               maxima through shared memory.
+//   warps 0-7   softmax of this CTA's 128 rows: warp w reads TMEM lanes
+//               32 (w % 4) .. + 31 (thread = row) and keys 128 (w / 4) .. + 127
+//               of the block into registers; the two warps of a row exchange
+//               their partial maxima through shared memory.
+// Two softmax warps per SM sub-partition (not four) leave the MMA-issuing
+// thread, which shares a sub-partition with two of them, enough issue slots
+// for the 64-cycle P V MMAs; with ten warps a thread may hold 168 registers,
+// enough for its 128 scores.
 // Rescaling is lazy: the reference max m_ref of a row moves (and O and l are
 // multiplied by exp2(m_ref_old - m_ref_new)) only when the block max exceeds
 // it by more than 8, so p <= 2^8.
@@ -69,8 +73,9 @@ constexpr int HD = 128;                      // head dim
 constexpr int STAGES = 2;
 constexpr int TILE_BYTES = 32768;            // Q tile, K half or V half
 constexpr int HALF_BYTES = 16384;            // one 64-column swizzled box of a 128-row tile
-constexpr int TMA_WARP = 16, MMA_WARP = 17;
-constexpr int THREADS = 18 * 32;
+constexpr int SM_WARPS = 8;                // softmax warps: two per TMEM lane quarter
+constexpr int TMA_WARP = 8, MMA_WARP = 9;
+constexpr int THREADS = 10 * 32;
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t S_COL = 0, P_COL = 256, O_COL = 384;
 constexpr float RESCALE_THRESHOLD = 8.0f;    // log2 units
@@ -88,8 +93,8 @@ struct Shared {
   uint64_t p_ready;             // CTA 0: both CTAs' P(g) and O rescale written (32 warps)
   uint64_t o_free;              // CTA 0: both CTAs' epilogues have read O (32 warps)
   uint64_t red_bar[4];          // each CTA, per lane quarter: its four warps' maxima / sums
-  float red[2][4][BM];          // [exchange & 1][key quarter][row]: partial row maxima
-  float part_l[4][BM];          // [key quarter][row]: partial row sums of an item
+  float red[2][2][BM];          // [exchange & 1][key half][row]: partial row maxima
+  float part_l[2][BM];          // [key half][row]: partial row sums of an item
   uint32_t tmem_base;
   int abort;
 };
@@ -201,10 +206,10 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     tc::mbar_init(&sh->s_full, 1);
     tc::mbar_init(&sh->pv_done, 1);
-    tc::mbar_init(&sh->s_free, 32);
-    tc::mbar_init(&sh->p_ready, 32);
-    tc::mbar_init(&sh->o_free, 32);
-    for (int q = 0; q < 4; ++q) tc::mbar_init(&sh->red_bar[q], 4);
+    tc::mbar_init(&sh->s_free, 2 * SM_WARPS);
+    tc::mbar_init(&sh->p_ready, 2 * SM_WARPS);
+    tc::mbar_init(&sh->o_free, 2 * SM_WARPS);
+    for (int q = 0; q < 4; ++q) tc::mbar_init(&sh->red_bar[q], 2);
     sh->abort = 0;
     tc::fence_barrier_init();
   }
@@ -342,7 +347,7 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   } else {
     // --------------------------------------------------- softmax ----
     const int quarter = warp & 3;                   // TMEM lanes 32 quarter .. + 31
-    const int kq = warp >> 2;                       // keys 64 kq .. + 63 of each block
+    const int kh = warp >> 2;                       // keys 128 kh .. + 127 of each block
     const int r = quarter * 32 + lane;              // this thread's row of the tile
     const uint32_t lanes = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t s_free0 = tc::mapa(tc::smem_u32(&sh->s_free), 0);
@@ -354,55 +359,48 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     bool ok = true;
     const long long heads = (long long)num_items / ((((N + BM - 1) / BM) + 1) / 2);
     (void)heads;                                    // read by the checked build only
-    // The epilogue of an item is deferred into the first block of the next:
-    // O is read there (once the item's last P V is done, which the new
-    // block's P has to wait for anyway), released for the next item's first
-    // P V, and written out after the new P is handed over.
     bool pend = false;                              // an item's output is still to be written
     float pend_m = 0.f, pend_l = 0.f;
-    int pend_row = 0;                               // global query row
-    bool pend_in = false;                           // the row belongs to a query
-    auto take_o = [&](uint32_t g_last, uint32_t (&v)[32]) -> bool {
-      if (!tc::mbar_wait(&sh->pv_done, g_last & 1u, abort)) return false;
-      tc::fence_after_sync();
-      tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kq * 32), v);
+    int pend_row = 0;
+    bool pend_in = false;
+    // O columns 64 kh .. + 63 of this thread's row
+    auto load_o = [&](uint32_t (&v)[64]) {
+      uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+      uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+      tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kh * 64), v0);
+      tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kh * 64 + 32), v1);
       tc::tmem_ld_wait();
-      // O is in registers: the next item's first P V may overwrite it
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) arrive_cluster_relaxed(o_free0);
-      return true;
     };
-    // the row's sum over its four warps; out = O / l and lse = (m_ref +
-    // log2 l) ln 2.  Warp (quarter, kq) writes columns 32 kq .. + 31 of rows
-    // 32 quarter .. + 31.
-    auto finish = [&](const uint32_t (&v)[32]) -> bool {
-      sh->part_l[kq][r] = pend_l;
+    auto finish = [&](const uint32_t (&v)[64]) -> bool {
+      sh->part_l[kh][r] = pend_l;
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->red_bar[quarter]);
       if (!tc::mbar_wait(&sh->red_bar[quarter], x & 1u, abort)) return false;
       ++x;
-      const float lt = (sh->part_l[0][r] + sh->part_l[1][r]) + (sh->part_l[2][r] + sh->part_l[3][r]);
+      const float lt = sh->part_l[0][r] + sh->part_l[1][r];
       const float inv = 1.f / lt;
-      uint32_t pkd[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        pkd[c] = pack_bf16x2(__uint_as_float(v[2 * c]) * inv, __uint_as_float(v[2 * c + 1]) * inv);
-      // (checked build) 32 outputs inside out[B*H][N][HD]
-      if (pend_in && RF_SPAN_OK((size_t)pend_row * HD + kq * 32, 32, heads * N * HD)) {
-        __nv_bfloat16* dst = out + (size_t)pend_row * HD + kq * 32;
-        if (out32) {
-          // 32-byte stores: each fills one sector of the row
-          st_global_v8(dst, pkd);
-          st_global_v8(dst + 16, pkd + 8);
-        } else {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pkd[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            d4[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+        for (int c = 0; c < 16; ++c)
+          pkd[c] = pack_bf16x2(__uint_as_float(v[32 * hh + 2 * c]) * inv,
+                               __uint_as_float(v[32 * hh + 2 * c + 1]) * inv);
+        const int col = kh * 64 + hh * 32;
+        if (pend_in && RF_SPAN_OK((size_t)pend_row * HD + col, 32, heads * N * HD)) {
+          __nv_bfloat16* dst = out + (size_t)pend_row * HD + col;
+          if (out32) {
+            st_global_v8(dst, pkd);
+            st_global_v8(dst + 16, pkd + 8);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              d4[c] = make_uint4(pkd[4 * c], pkd[4 * c + 1], pkd[4 * c + 2], pkd[4 * c + 3]);
+          }
         }
       }
-      if (lse != nullptr && kq == 0 && pend_in && RF_IDX_OK(pend_row, heads * N))
+      if (lse != nullptr && kh == 0 && pend_in && RF_IDX_OK(pend_row, heads * N))
         lse[pend_row] = (pend_m + log2f(lt)) * kLn2;
       return true;
     };
@@ -410,71 +408,56 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const int i = item_index(t, cluster, nclusters);
       if (i >= num_items) break;
       const Item it = item_of(i, N, causal);
-      const int m_tile = 2 * it.pair + rank;        // this CTA's query tile
+      const int m_tile = 2 * it.pair + rank;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < it.n; ++j, ++g) {
         if (!(ok = tc::mbar_wait(&sh->s_full, g & 1u, abort))) break;
         tc::fence_after_sync();
-        float s[64];                                // s[c] = key 64 kq + c of block j
+        float s[128];                               // s[c] = key 128 kh + c of block j
         {
-          uint32_t v[32], u[32];
-          tc::tmem_ld_32x32b_x32(lanes + S_COL + (uint32_t)(kq * 64), v);
-          tc::tmem_ld_32x32b_x32(lanes + S_COL + (uint32_t)(kq * 64 + 32), u);
-          tc::tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            s[c] = __uint_as_float(v[c]);
-            s[32 + c] = __uint_as_float(u[c]);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t (&v)[32] = *reinterpret_cast<uint32_t(*)[32]>(&s[32 * q4]);
+            tc::tmem_ld_32x32b_x32(lanes + S_COL + (uint32_t)(kh * 128 + 32 * q4), v);
           }
+          tc::tmem_ld_wait();
         }
-        // S(g) is in registers: the MMA thread may overwrite it with S(g + 1)
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) arrive_cluster_relaxed(s_free0);
         if (causal && j == it.n - 1) {
-          // the block on the diagonal: key 256 pair + 64 kq + c against query
-          // row 256 pair + 128 rank + r
-          const int lim = BM * rank + r - kq * 64;
+          const int lim = BM * rank + r - kh * 128;
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 128; ++c)
             if (c > lim) s[c] = -INFINITY;
         } else if (!causal && j == NKB - 1 && N % BN != 0) {
-          // keys past N in the last block are the next head's rows (or TMA's
-          // zero fill): leave them out.  Under the causal mask they never
-          // count for a row that is stored.
-          const int kmax = N - j * BN - kq * 64;
+          const int kmax = N - j * BN - kh * 128;
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 128; ++c)
             if (c >= kmax) s[c] = -INFINITY;
         }
-        // row max: this thread's 64 keys (three-input max), then the four
-        // warps of the row through shared memory; raw scores (scale_log2 > 0
-        // is applied after)
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) mx[(c >> 1) & 3] = max3(mx[(c >> 1) & 3], s[c], s[c + 1]);
+        for (int c = 0; c < 128; c += 2) mx[(c >> 1) & 3] = max3(mx[(c >> 1) & 3], s[c], s[c + 1]);
         float* red = &sh->red[x & 1u][0][0];
-        red[kq * BM + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        red[kh * BM + r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sh->red_bar[quarter]);
         if (!(ok = tc::mbar_wait(&sh->red_bar[quarter], x & 1u, abort))) break;
         ++x;
-        const float pm = fmaxf(fmaxf(red[r], red[BM + r]), fmaxf(red[2 * BM + r], red[3 * BM + r]));
+        const float pm = fmaxf(red[r], red[BM + r]);
         const float mt = pm * scale_log2;
-        // move the reference max only when it has grown by more than the threshold
         const bool move = mt > m_ref + RESCALE_THRESHOLD;
         const float m_new = move ? mt : m_ref;
-        const float alpha = ex2(m_ref - m_new);     // 0 on the first block, 1 when not moved
+        const float alpha = ex2(m_ref - m_new);
         l *= alpha;
         m_ref = m_new;
-        // P = exp2(s scale_log2 - m) as bf16 pairs, row sums on pairs (packed
-        // fp32x2 FMA and add)
-        uint32_t w[32];
+        uint32_t w[64];
         {
           const uint64_t nm2 = pack_f32x2(-m_new, -m_new);
           uint64_t sum2 = 0ull;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < 64; ++c) {
             float a0, a1;
             unpack_f32x2(fma_f32x2(pack_f32x2(s[2 * c], s[2 * c + 1]), sl2, nm2), a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
@@ -485,37 +468,37 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           unpack_f32x2(sum2, s0, s1);
           l += s0 + s1;
         }
-        // P and O are free once the previous P V is done: within an item
-        // wait for it here (and rescale O when a row's reference moved); the
-        // first block of an item follows the last item's epilogue, which
-        // waited for it
         if (j > 0) {
           if (!(ok = tc::mbar_wait(&sh->pv_done, (g - 1) & 1u, abort))) break;
           tc::fence_after_sync();
           if (__any_sync(0xffffffffu, move)) {
-            const uint32_t oc = lanes + O_COL + (uint32_t)(kq * 32);
-            uint32_t v[32];
-            tc::tmem_ld_32x32b_x32(oc, v);
-            tc::tmem_ld_wait();
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t oc = lanes + O_COL + (uint32_t)(kh * 64 + hh * 32);
+              uint32_t v[32];
+              tc::tmem_ld_32x32b_x32(oc, v);
+              tc::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
-            tc::tmem_st_32x32b_x32(oc, v);
+              for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * alpha);
+              tc::tmem_st_32x32b_x32(oc, v);
+            }
           }
         }
         const bool have_o = j == 0 && pend;
         if (have_o) {
-          // P and O are the previous item's until its last P V is done
           if (!(ok = tc::mbar_wait(&sh->pv_done, (g - 1) & 1u, abort))) break;
           tc::fence_after_sync();
         }
-        tc::tmem_st_32x32b_x32(lanes + P_COL + (uint32_t)(kq * 32), w);
+        {
+          uint32_t (&w0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[0]);
+          uint32_t (&w1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&w[32]);
+          tc::tmem_st_32x32b_x32(lanes + P_COL + (uint32_t)(kh * 64), w0);
+          tc::tmem_st_32x32b_x32(lanes + P_COL + (uint32_t)(kh * 64 + 32), w1);
+        }
         tc::tmem_st_wait();
         if (have_o) {
-          uint32_t ov[32];                          // the previous item's O
-          tc::tmem_ld_32x32b_x32(lanes + O_COL + (uint32_t)(kq * 32), ov);
-          tc::tmem_ld_wait();
-          // O is in registers and P is written: the first P V of this item
-          // may go
+          uint32_t ov[64];
+          load_o(ov);
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) {
@@ -535,11 +518,18 @@ prefill_2sm_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       pend_m = m_ref;
       pend_l = l;
       pend_row = it.key0 + m_tile * BM + r;
-      pend_in = m_tile * BM + r < N;              // rows past N belong to no query
+      pend_in = m_tile * BM + r < N;
     }
     if (ok && pend) {
-      uint32_t ov[32];
-      if (take_o(g - 1, ov)) finish(ov);
+      if (tc::mbar_wait(&sh->pv_done, (g - 1) & 1u, abort)) {
+        tc::fence_after_sync();
+        uint32_t ov[64];
+        load_o(ov);
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) arrive_cluster_relaxed(o_free0);
+        finish(ov);
+      }
     }
   }
 

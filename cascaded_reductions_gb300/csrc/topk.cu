@@ -562,7 +562,13 @@ softmax_top2_row_kernel(const float* __restrict__ logits, int T, int k, int reno
 // 16-byte chunks [32 h, 32 h + 32) of the row; chunk C of row t lands at
 // position C ^ (2 (t & 3) + C / 32), so the 8-thread phases of the 16-byte
 // loads (four tokens x two halves reading the same chunk offset) hit 8
-// different bank groups.  Per token:
+// different bank groups.  The copies go out in eight commit groups by
+// column, group g holding chunks 32 h + 4 g .. 32 h + 4 g + 3 of every row
+// (the thread's value group g, below), and each thread takes the maximum of
+// group g as soon as that commit group has landed, while the later ones are
+// still in flight ([16384 x 256] top-8: 7.47 -> 7.33 us in a CUDA graph over
+// copies larger than L2; 9.95 -> 8.89 us in a loop of plain launches).  Per
+// token:
 //   * each thread takes the maxima of its 8 groups of 16 values and sorts
 //     them; the 8 largest of the pair's 16 are max(mine[i], partner[7-i])
 //     (one shuffle each), and thr, the smallest of those, has at least 8
@@ -592,16 +598,22 @@ softmax_top8_pair_kernel(const float* __restrict__ logits, int T, int k_rt,
   const int t0 = blockIdx.x * TOK;
   const int nrows = min(TOK, T - t0);
   const float4* src = reinterpret_cast<const float4*>(logits) + (size_t)t0 * CH;
-  for (int q = threadIdx.x; q < nrows * CH; q += 32) {
-    const int t = q / CH, c = q % CH;
-    if (RF_SPAN_OK(((size_t)t0 * CH + q) * 4, 4, (long long)T * E)) {
-      const int f = ((t & 3) << 1) | (c >> 5);
-      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&rows[t * CH + (c ^ f)]);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + q) : "memory");
+#pragma unroll
+  for (int kq = 0; kq < 8; ++kq) {     // commit group kq: chunks 4 kq .. 4 kq + 3 of each half
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int q2 = threadIdx.x + 32 * i;
+      const int t = q2 >> 3, lc = q2 & 7;
+      const int c = ((lc >> 2) << 5) + 4 * kq + (lc & 3);
+      if (t < nrows && RF_SPAN_OK(((size_t)t0 * CH + t * CH + c) * 4, 4, (long long)T * E)) {
+        const int f = ((t & 3) << 1) | (c >> 5);
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&rows[t * CH + (c ^ f)]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + t * CH + c)
+                     : "memory");
+      }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  __syncthreads();
   // pairs past the last row work on the last row (the shuffles need every
   // lane) and store nothing
   const int tl = min(threadIdx.x >> 1, nrows - 1), h = threadIdx.x & 1;
@@ -611,14 +623,23 @@ softmax_top8_pair_kernel(const float* __restrict__ logits, int T, int k_rt,
   // maxima of the thread's 8 groups of 16 values, sorted descending
   float sm[8];
 #pragma unroll
-  for (int g = 0; g < 8; ++g) {
+  for (int kq = 0; kq < 8; ++kq) {
+    if (kq == 0) asm volatile("cp.async.wait_group 7;" ::: "memory");
+    if (kq == 1) asm volatile("cp.async.wait_group 6;" ::: "memory");
+    if (kq == 2) asm volatile("cp.async.wait_group 5;" ::: "memory");
+    if (kq == 3) asm volatile("cp.async.wait_group 4;" ::: "memory");
+    if (kq == 4) asm volatile("cp.async.wait_group 3;" ::: "memory");
+    if (kq == 5) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    if (kq == 6) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    if (kq == 7) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();     // the block is one warp: the other lanes' copies are visible
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float4 v = row[(32 * h + 4 * g + j) ^ f];
+      const float4 v = row[(32 * h + 4 * kq + j) ^ f];
       m = max3f(m, max3f(v.x, v.y, v.z), v.w);
     }
-    sm[g] = m;
+    sm[kq] = m;
   }
   auto cs = [](float& a, float& b) {
     const float hi = fmaxf(a, b), lo = fminf(a, b);

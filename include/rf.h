@@ -222,8 +222,10 @@ rf_status rf_softmax_topk(const float* logits, int T, int E, int k, int renormal
  *   sx   [M]     fp32 out       per-token scales
  *   y    [M, N]  bf16 out
  * Any M, N >= 1; K a multiple of 16 (16-byte code rows) up to 65536.  The
- * GEMM works on 128 x 256 output tiles; partial tiles at the M, N and K
- * edges read zeros past the edge and store only inside Y.
+ * GEMM works on 256 x 256 output tiles, each computed by a cluster of two
+ * CTAs (128 x 256 tiles on single CTAs when M <= 128 or when such a cluster
+ * cannot be launched on the device); partial tiles at the
+ * M, N and K edges read zeros past the edge and store only inside Y.
  * Errors: RF_ERR_INVALID_ARG for null pointers or sizes <= 0;
  * RF_ERR_UNSUPPORTED unless K % 16 == 0 and K <= 65536; RF_ERR_MISALIGNED
  * unless x, wq, sw, xq and y are 16-byte aligned.
